@@ -1,0 +1,414 @@
+#!/usr/bin/env python3
+"""Ring-attention fwd+bwd throughput on GB300 (useful causal TFLOP/s).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step = the whole hot path on one batch: ring forward (all ring steps,
+exact log-sum-exp merge, bf16 output) then ring backward (Delta preprocess,
+all ring steps, bf16 gradients), on seeded synthetic bf16 inputs resident in
+HBM.  Useful FLOPs count visible (query, key) pairs only: forward 4 d Hq P,
+backward 10 d Hq P (P = sum over documents of L(L+1)/2 when causal).
+
+With N > 1 (torchrun, one process per GPU) every rank runs an independent
+replica of the same workload ("replicas only": on one GPU per box the ring has
+no inter-GPU exchange); value = all ranks' FLOPs / max-over-ranks time.
+
+--impl reference times the fp64 CPU oracle on a bounded sample of the same
+workload on the host cores (rank 0 only).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "ring-attn fwd+bwd TFLOP/s (useful, causal) on 1 GB300; % of BF16 dense peak"
+
+
+def visible_pairs(wl):
+    return sum(L * (L + 1) // 2 if wl.causal else L * L for L in wl.doc_lengths)
+
+
+def useful_flops(wl, pairs=None):
+    P = visible_pairs(wl) if pairs is None else pairs
+    return 4.0 * wl.d * wl.Hq * P, 10.0 * wl.d * wl.Hq * P
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), float(m["hbm_gbs"]), "measured"
+    except Exception:
+        return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def step_pairs_bwd(items, off, causal):
+    """Visible (query, key) pairs processed by each backward ring-step launch."""
+    import numpy as np
+    out = []
+    for s in range(len(off) - 1):
+        tot = 0
+        for k0, k1, qb0, qe0, qb1, qe1, _, _ in items[off[s]:off[s + 1]]:
+            keys = np.arange(k0, k1)
+            for qb, qe in ((qb0, qe0), (qb1, qe1)):
+                if qe <= qb:
+                    continue
+                if causal:  # queries q in [qb, qe) with q >= k
+                    tot += int(np.clip(qe - np.maximum(qb, keys), 0, None).sum())
+                else:
+                    tot += (k1 - k0) * (qe - qb)
+        out.append(tot)
+    return out
+
+
+def step_pairs_fwd(items, off, causal):
+    """Visible (query, key) pairs processed by each forward ring-step launch."""
+    import numpy as np
+    out = []
+    for s in range(len(off) - 1):
+        tot = 0
+        for q0, q1, kb0, ke0, kb1, ke1, _, _ in items[off[s]:off[s + 1]]:
+            rows = np.arange(q0, q1)
+            for kb, ke in ((kb0, ke0), (kb1, ke1)):
+                if ke <= kb:
+                    continue
+                if causal:  # keys k in [kb, ke) with k <= q
+                    tot += int(np.clip(np.minimum(rows + 1, ke) - kb, 0, None).sum())
+                else:
+                    tot += (q1 - q0) * (ke - kb)
+        out.append(tot)
+    return out
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.QUERY,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def cpu_oracle_sample(wl, q, k, v, do, tokens):
+    """fp64 oracle fwd+bwd on a causal prefix of `tokens` tokens of query head 0."""
+    from oracle import attention as A
+    import torch
+    Tn = min(tokens, wl.doc_lengths[0])
+    qs, ks, vs, dos = (x[:Tn] for x in (q, k, v, do))
+    qs = qs[:, :1].contiguous()
+    dos = dos[:, :1].contiguous()
+    ks = ks[:, :1].contiguous()
+    vs = vs[:, :1].contiguous()
+    t0 = time.perf_counter()
+    A.attention_bwd(qs, ks, vs, dos, [0, Tn], wl.causal, wl.softmax_scale)
+    dt = time.perf_counter() - t0
+    P = Tn * (Tn + 1) // 2 if wl.causal else Tn * Tn
+    flops = 14.0 * wl.d * 1 * P
+    del torch
+    return flops, dt, "causal prefix of %d tokens of document 0, query head 0 / kv head 0, fwd+bwd in float64" % Tn
+
+
+def blas_threads():
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return os.cpu_count() or 1
+
+
+def run_reference(args, wl):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    from workloads import draw_qkvdo
+    q, k, v, do = draw_qkvdo(wl)
+    tokens = args.cpu_tokens
+    for _ in range(args.warmup):
+        cpu_oracle_sample(wl, q, k, v, do, min(tokens, 2048))
+    times, flops, sample = [], 0.0, ""
+    for _ in range(args.steps):
+        flops, dt, sample = cpu_oracle_sample(wl, q, k, v, do, tokens)
+        times.append(dt)
+    tot = sum(times)
+    value = flops * len(times) / tot / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * tot / len(times),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": config_of(wl),
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def config_of(wl):
+    return {"workload": wl.name, "T": wl.T, "Hq": wl.Hq, "Hkv": wl.Hkv, "head_dim": wl.d,
+            "cp_size": max(wl.cp_per_doc), "layout": wl.layout, "causal": wl.causal,
+            "docs": wl.num_docs, "seed": wl.seed,
+            "l2": "inputs larger than L2 (q, dO 1 GiB each at 128K), no flush"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="long_128k")
+    ap.add_argument("--e2e-steps", type=int, default=2)
+    ap.add_argument("--cpu-tokens", type=int, default=12288)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    from workloads import workload
+    wl = workload(args.workload)
+    if args.impl == "reference":
+        return run_reference(args, wl)
+
+    import torch
+    import torch.distributed as dist
+    import context_ring_attention_step_gb300 as ra
+    from workloads import draw_qkvdo
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    lib = ra.load_library()
+
+    q_h, k_h, v_h, do_h = draw_qkvdo(wl)
+    cps = list(wl.cp_per_doc)
+    plan = ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    steps = plan.stats()["steps"]
+    q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
+    T, Hq, Hkv, D = wl.T, wl.Hq, wl.Hkv, wl.d
+    o = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    dq = torch.empty((T, Hq, D), dtype=torch.bfloat16, device=dev)
+    dk = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    dv = torch.empty((T, Hkv, D), dtype=torch.bfloat16, device=dev)
+    wf, wb = plan.workspace_bytes(False, False)
+    ws_f = torch.empty(wf, dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(wb, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = ra.ring_attn._stream(dev)
+    P_ = ra.ring_attn._ptr
+    H = plan.handle
+    fitems, foff = plan.work_items("fwd")
+    bitems, boff = plan.work_items("bwd")
+    fpairs = step_pairs_fwd(fitems, foff, wl.causal)
+    bpairs = step_pairs_bwd(bitems, boff, wl.causal)
+    fwd_launches = sum(1 for s in range(steps) if foff[s + 1] > foff[s])
+    bwd_launches = sum(1 for s in range(steps) if boff[s + 1] > boff[s])
+
+    def chk(st):
+        if st != 0:
+            raise RuntimeError("ring_attn status %d: %s" % (st, lib.ra_last_error().decode()))
+
+    def events():
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+
+    def one_step(ev_f=None, ev_b=None):
+        chk(lib.ra_fwd_prepare(H, 0, P_(ws_f), wf, sp))
+        for s in range(steps):
+            if ev_f:
+                ev_f[s][0].record(stream)
+            chk(lib.ra_fwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(o), 0, P_(lse), P_(ws_f), wf, sp))
+            if ev_f:
+                ev_f[s][1].record(stream)
+        chk(lib.ra_fwd_finish(H, P_(o), 0, P_(ws_f), wf, sp))
+        chk(lib.ra_bwd_prepare(H, P_(o), 0, P_(do), P_(lse), P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb, sp))
+        for s in range(steps):
+            if ev_b:
+                ev_b[s][0].record(stream)
+            chk(lib.ra_bwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(do), P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb,
+                                     sp))
+            if ev_b:
+                ev_b[s][1].record(stream)
+        chk(lib.ra_bwd_finish(H, P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb, sp))
+
+    for _ in range(args.warmup):
+        one_step()
+    torch.cuda.synchronize()
+    chk(lib.ra_workspace_status(P_(ws_f), sp))
+    chk(lib.ra_workspace_status(P_(ws_b), sp))
+
+    # ---------------------------------------------------------------- timed region
+    t_f = [0.0] * steps
+    t_b = [0.0] * steps
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    evs = [(events(), events()) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        e0.record(stream)
+        for it in range(args.steps):
+            one_step(*evs[it])
+        e1.record(stream)
+        torch.cuda.synchronize()
+    for ev_f, ev_b in evs:
+        for s in range(steps):
+            if foff[s + 1] > foff[s]:
+                t_f[s] += ev_f[s][0].elapsed_time(ev_f[s][1])
+            if boff[s + 1] > boff[s]:
+                t_b[s] += ev_b[s][0].elapsed_time(ev_b[s][1])
+    ms_total = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+        dist.barrier()
+    chk(lib.ra_workspace_status(P_(ws_f), sp))
+    chk(lib.ra_workspace_status(P_(ws_b), sp))
+
+    ff, fb = useful_flops(wl)
+    ms_step = ms_total / args.steps
+    value = world * (ff + fb) * args.steps / (ms_total * 1e-3) / 1e12
+    peak_b, peak_s, hbm, peak_kind = peaks()
+    fwd_ms = sum(t_f) / args.steps
+    bwd_ms = sum(t_b) / args.steps
+
+    # roofline of the dominant kernel (per-launch events on the launching stream)
+    if sum(t_b) >= sum(t_f):
+        name, tot_ms, launches, pairs, per_pair = "ring_bwd_step_kernel", sum(t_b), bwd_launches, bpairs, 10.0
+    else:
+        name, tot_ms, launches, pairs, per_pair = "ring_fwd_step_kernel", sum(t_f), fwd_launches, fpairs, 4.0
+    alg_flops_per_launch = per_pair * wl.d * wl.Hq * sum(pairs) / max(1, launches)
+    avg_launch_s = tot_ms * 1e-3 / (args.steps * max(1, launches))
+    achieved = alg_flops_per_launch / avg_launch_s / 1e12
+    roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak_s, "unit": "TFLOP/s",
+            "frac": achieved / peak_s, "peak_kind": peak_kind + " bf16 sustained (kernel timed inside a long step)",
+            "frac_of_burst_peak": achieved / peak_b, "traffic": None,
+            "per_launch_flops": alg_flops_per_launch, "avg_launch_ms": avg_launch_s * 1e3}
+
+    # ---------------------------------------------------------------- end to end (host buffers)
+    e2e = None
+    if args.e2e_steps > 0:
+        pin = [x.pin_memory() for x in (q_h, k_h, v_h, do_h)]
+        outs_h = [torch.empty((T, Hq, D), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((Hq, T), dtype=torch.float32).pin_memory(),
+                  torch.empty((T, Hq, D), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory(),
+                  torch.empty((T, Hkv, D), dtype=torch.bfloat16).pin_memory()]
+        h2d = sum(x.numel() * x.element_size() for x in pin)
+        d2h = sum(x.numel() * x.element_size() for x in outs_h)
+        torch.cuda.synchronize()
+        if world > 1:
+            dist.barrier()
+        a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for _ in range(args.e2e_steps):
+            qd, kd, vd, dod = (x.to(dev, non_blocking=True) for x in pin)
+            oo, ll = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale,
+                                      plan=plan, workspace=ws_f)
+            gq, gk, gv = ra.ring_attn_bwd(qd, kd, vd, oo, dod, ll, wl.cu_seqlens, cps, wl.layout, wl.causal,
+                                          wl.softmax_scale, plan=plan, workspace=ws_b)
+            for dst, src in zip(outs_h, (oo, ll, gq, gk, gv)):
+                dst.copy_(src, non_blocking=True)
+        a1.record(stream)
+        torch.cuda.synchronize()
+        e_ms = a0.elapsed_time(a1)
+        if world > 1:
+            t = torch.tensor([e_ms], device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e_ms = float(t.item())
+        e2e = {"value": world * (ff + fb) * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+               "ms_per_step": e_ms / args.e2e_steps}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        flops, dt, sample = cpu_oracle_sample(wl, q_h, k_h, v_h, do_h, args.cpu_tokens)
+        cpu = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
+               "sample": sample, "seconds": dt}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(wl),
+            "pct_of_bf16_peak": 100.0 * value / world / peak_b, "pct_of_bf16_peak_sustained":
+                100.0 * value / world / peak_s,
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "fwd_tflops": ff / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
+            "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
+            "useful_flops_per_step": ff + fb, "strict_bwd_flops_per_step": 0.8 * fb,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3),
+            "clocks": clk.summary(),
+        }
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,401 @@
+// fwd.cu -- one ring step of the forward pass on tcgen05 tensor cores.
+//
+// One CTA takes up to 256 query rows (two 128-row tiles Q0, Q1) of one head and
+// runs the online softmax over the key/value tiles of the shard its query
+// shard holds at this ring step (NVSHMEM/XLA page, "Paralelismo de contexto y
+// atencion en anillo": attention is computed incrementally as KV blocks
+// circulate).  The step's partial (O_s, LSE_s) is merged exactly into the
+// running (O, LSE) in the epilogue (the Accelerate guide's `combine`, read as
+// the log-sum-exp merge).
+//
+// Warp roles (384 threads):
+//   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of stages
+//   warp 1      TMEM owner + single-thread UMMA issuer
+//   warps 4-7   softmax / correction / epilogue of Q0 (TMEM lanes 0-127)
+//   warps 8-11  softmax / correction / epilogue of Q1
+// Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after that.
+// P (bf16) overwrites the first 64 columns of S and feeds the P.V MMA straight
+// from tensor memory.  MMA order per key tile j: PV0(j), S0(j+1), PV1(j),
+// S1(j+1), so one Q tile's softmax overlaps the other tile's MMAs.
+#include "ring_attn_internal.h"
+#include "tc.cuh"
+
+namespace ra {
+namespace {
+
+#define kNegInf (-__int_as_float(0x7f800000))
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
+
+template <int D>
+struct FwdCfg {
+  static constexpr int kTile = 128 * D * 2;  // bytes of one 128-row bf16 tile
+  static constexpr int kStages = D == 128 ? 4 : 8;
+  static constexpr int kQBytes = 2 * kTile;
+  static constexpr int kKVBytes = kStages * kTile;
+  static constexpr int kBarOff = kQBytes + kKVBytes;
+  static constexpr int kSmem = kBarOff + 512 + 1024;  // barriers + alignment slack
+  static constexpr uint32_t kIdescQK = idesc_bf16_f32(128, 128, false, false);
+  static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
+};
+
+struct TileList {
+  int32_t kb0, ke0, kb1, ke1, n0, n;
+  __device__ __forceinline__ int start(int j) const { return j < n0 ? kb0 + 128 * j : kb1 + 128 * (j - n0); }
+  __device__ __forceinline__ int end(int j) const { return j < n0 ? ke0 : ke1; }
+};
+
+__device__ __forceinline__ int ceil128(int a, int b) { return b > a ? (b - a + 127) / 128 : 0; }
+
+template <int D>
+__global__ void __launch_bounds__(384, 1)
+    ring_fwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                         const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
+  using C = FwdCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sQ = smem_u32(smem);
+  const uint32_t sKV = sQ + C::kQBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBarOff);
+  // barrier map
+  const uint32_t b_q = smem_u32(bars + 0);
+  const uint32_t b_full = smem_u32(bars + 1);                      // [kStages]
+  const uint32_t b_empty = smem_u32(bars + 1 + C::kStages);        // [kStages]
+  const uint32_t b_s = smem_u32(bars + 1 + 2 * C::kStages);        // [2] S ready / O final
+  const uint32_t b_p = smem_u32(bars + 3 + 2 * C::kStages);        // [2] P written
+  const uint32_t b_drain = smem_u32(bars + 5 + 2 * C::kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6 + 2 * C::kStages);
+  int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
+
+  // A CTA of this grid already gave up: do no work (fail fast, no waits).
+  if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.x % p.Hq;
+  const int g = h / (p.Hq / p.Hkv);
+  const FwdItem it = p.items[blockIdx.x / p.Hq];
+
+  TileList tl;
+  tl.kb0 = it.kb0; tl.ke0 = it.ke0; tl.kb1 = it.kb1; tl.ke1 = it.ke1;
+  tl.n0 = ceil128(it.kb0, it.ke0);
+  tl.n = tl.n0 + ceil128(it.kb1, it.ke1);
+  // active key tiles of each Q tile form a prefix of the tile list
+  int n_act[2];
+  bool q_act[2];
+#pragma unroll
+  for (int qt = 0; qt < 2; ++qt) {
+    const int first = it.q0 + 128 * qt;
+    q_act[qt] = first < it.q1;
+    const int last = min(first + 128, it.q1) - 1;
+    int n = 0;
+    if (q_act[qt]) {
+      if (!p.causal) n = tl.n;
+      else while (n < tl.n && tl.start(n) <= last) ++n;
+    }
+    n_act[qt] = n;
+  }
+
+  if (threadIdx.x == 0) {
+    mbar_init(b_q, 1);
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(b_full + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 1);
+    }
+    mbar_init(b_s, 1); mbar_init(b_s + 8, 1);
+    mbar_init(b_p, 128); mbar_init(b_p + 8, 128);
+    mbar_init(b_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const Abort ab{abort_flag, p.status};
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV);
+      mbar_expect_tx(b_q, (q_act[0] ? C::kTile : 0) + (q_act[1] ? C::kTile : 0));
+      for (int qt = 0; qt < 2; ++qt) {
+        if (!q_act[qt]) continue;
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_3d(sQ + qt * C::kTile + hf * 16384, &tmQ, b_q, 64 * hf, h, it.q0 + 128 * qt);
+      }
+      int issued = 0;
+      bool ok = true;
+      for (int j = 0; j < tl.n && ok; ++j) {
+        for (int kind = 0; kind < 2; ++kind) {
+          const int st = issued % C::kStages;
+          const uint32_t ph = (issued / C::kStages) & 1;
+          if (!mbar_wait(b_empty + 8 * st, ph ^ 1, ab, 101)) { ok = false; break; }
+          mbar_expect_tx(b_full + 8 * st, C::kTile);
+          const CUtensorMap* m = kind == 0 ? &tmK : &tmV;
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_3d(sKV + st * C::kTile + hf * 16384, m, b_full + 8 * st, 64 * hf, g, tl.start(j));
+          ++issued;
+        }
+      }
+      if (!ok) {  // drain this CTA's copies still in flight
+        mbar_wait_drain(b_q, 0);
+        for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
+          mbar_wait_drain(b_full + 8 * (i % C::kStages), (i / C::kStages) & 1);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      bool ok = mbar_wait(b_q, 0, ab, 102);
+      tc_fence_after();
+      int stage = 0;
+      uint32_t kph = 0;
+      auto advance = [&]() { if (++stage == C::kStages) { stage = 0; kph ^= 1; } };
+      auto qk = [&](int qt, int kst) {
+        const uint32_t qa = sQ + qt * C::kTile, ka = sKV + kst * C::kTile;
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+          umma_ss(tmem + qt * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
+                  C::kIdescQK, kk > 0);
+        }
+      };
+      if (ok) ok = mbar_wait(b_full + 8 * stage, kph, ab, 103);
+      if (ok) {
+        tc_fence_after();
+        for (int qt = 0; qt < 2; ++qt)
+          if (n_act[qt] > 0) { qk(qt, stage); umma_commit(b_s + 8 * qt); }
+        umma_commit(b_empty + 8 * stage);
+        advance();
+      }
+      uint32_t pph0 = 0, pph1 = 0;
+      const int na0 = n_act[0], na1 = n_act[1];
+      for (int j = 0; j < tl.n && ok; ++j) {
+        const int vst = stage;
+        if (!mbar_wait(b_full + 8 * vst, kph, ab, 104)) { ok = false; break; }
+        tc_fence_after();
+        advance();  // stage now holds K_{j+1}
+        bool k_ready = false;
+        auto pv_then_qk = [&](int qt, int na, uint32_t& pph) {
+          if (!ok || j >= na) return;
+          if (!mbar_wait(b_p + 8 * qt, pph, ab, 105)) { ok = false; return; }
+          pph ^= 1;
+          tc_fence_after();
+          const uint32_t va = sKV + vst * C::kTile;
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tmem + 256 + qt * D, tmem + qt * 128 + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024),
+                    C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          if (j + 1 < na) {
+            if (!k_ready) {
+              if (!mbar_wait(b_full + 8 * stage, kph, ab, 106)) { ok = false; return; }
+              tc_fence_after();
+              k_ready = true;
+            }
+            qk(qt, stage);
+          }
+          umma_commit(b_s + 8 * qt);  // S(j+1) ready, or O final after the last tile
+        };
+        pv_then_qk(0, na0, pph0);
+        pv_then_qk(1, na1, pph1);
+        if (!ok) break;
+        umma_commit(b_empty + 8 * vst);
+        if (j + 1 < tl.n) {
+          if (!k_ready) {
+            if (!mbar_wait(b_full + 8 * stage, kph, ab, 107)) { ok = false; break; }
+          }
+          umma_commit(b_empty + 8 * stage);
+          advance();
+        }
+      }
+      if (!ok) {  // let issued MMAs finish before tensor memory is released
+        umma_commit(b_drain);
+        mbar_wait_drain(b_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int qt = (warp - 4) >> 2;
+    const int tid = threadIdx.x - 128 * (1 + qt);
+    const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
+    const uint32_t tS = tmem_addr(tmem, lane_base, qt * 128);
+    const uint32_t tO = tmem_addr(tmem, lane_base, 256 + qt * D);
+    const int row0 = it.q0 + 128 * qt;
+    const int row = row0 + tid;
+    const float sl2 = p.scale_log2;
+    float m_ref = kNegInf, l_sum = 0.f;
+    uint32_t sph = 0;
+    bool ok = true;
+    const int na = qt == 0 ? n_act[0] : n_act[1];
+    const bool qa = qt == 0 ? q_act[0] : q_act[1];
+    for (int j = 0; j < na; ++j) {
+      if (!mbar_wait(b_s + 8 * qt, sph, ab, 110)) { ok = false; break; }
+      sph ^= 1;
+      tc_fence_after();
+      uint32_t r[4][32];
+      tmem_ld32(tS + 0, r[0]);
+      tmem_ld32(tS + 32, r[1]);
+      tmem_ld32(tS + 64, r[2]);
+      tmem_ld32(tS + 96, r[3]);
+      tmem_ld_wait();
+      reg_fence32(r[0]); reg_fence32(r[1]); reg_fence32(r[2]); reg_fence32(r[3]);
+      const int kst = tl.start(j), kend = tl.end(j);
+      const bool need_mask = (kst + 128 > kend) || (p.causal && kst + 127 > row0);
+      if (need_mask) {
+        const int lim = p.causal ? min(kend - 1, row) : kend - 1;
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kst + c > lim) r[c >> 5][c & 31] = __float_as_uint(kNegInf);
+      }
+      float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        mx0 = fmaxf(mx0, __uint_as_float(r[0][c]));
+        mx1 = fmaxf(mx1, __uint_as_float(r[1][c]));
+        mx2 = fmaxf(mx2, __uint_as_float(r[2][c]));
+        mx3 = fmaxf(mx3, __uint_as_float(r[3][c]));
+      }
+      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float m_new = fmaxf(m_ref, m_tile);
+      const bool rescale = m_new > m_ref + kRescaleThreshold;
+      float alpha = 1.f;
+      if (rescale) {
+        // The reference max is kept integral (log2 units): partials over any split
+        // of the keys then differ by exact powers of two, so the bf16 rounding of P
+        // does not depend on the ring layout.
+        const float m_int = ceilf(m_new);
+        alpha = ex2_approx(m_ref - m_int);
+        l_sum *= alpha;
+        m_ref = m_int;
+      }
+      const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
+      float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i]), sl2, -m_use));
+          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i + 1]), sl2, -m_use));
+          ls0 += p0;
+          ls1 += p1;
+          pk[i] = pack_bf16x2(p0, p1);
+        }
+        tmem_st16(tS + 16 * c, pk);
+      }
+      l_sum += ls0 + ls1;
+      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1));
+        // P is already stored, so the S registers are free here.
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(tO + 32 * c, o);
+          tmem_ld_wait();
+          reg_fence32(o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(tO + 32 * c, o);
+        }
+        tmem_st_wait();
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_p + 8 * qt);
+    }
+    if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
+      if (na > 0) {
+        ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
+        tc_fence_after();
+      }
+      if (ok) {
+        const bool valid = row < it.q1;
+        const bool first = (it.flags & kFirstStep) != 0;
+        const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
+        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+        float* lse_ptr = p.lse + (size_t)h * p.T + row;
+        float* orow = p.o_run + ((size_t)row * p.Hq + h) * D;
+        const float lse_a = (valid && !first) ? *lse_ptr : kNegInf;
+        float wa = 0.f, wb = 1.f, lse_new = lse_b;
+        if (lse_b == kNegInf) { wa = 1.f; wb = 0.f; lse_new = lse_a; }
+        else if (lse_a != kNegInf) {
+          const float a2 = lse_a * 1.4426950408889634f, b2 = lse_b * 1.4426950408889634f;
+          const float mx = fmaxf(a2, b2);
+          const float n2 = mx + log2f(1.f + exp2f(-fabsf(a2 - b2)));
+          wa = exp2f(a2 - n2);
+          wb = exp2f(b2 - n2);
+          lse_new = n2 * kLn2;
+        }
+        wb *= inv_l;
+        const bool write = valid && (first || lse_b != kNegInf);
+        const bool read_old = valid && !first && lse_a != kNegInf && lse_b != kNegInf;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (na > 0) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (write) {
+            float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              float4 v;
+              v.x = __uint_as_float(o[4 * i + 0]) * wb;
+              v.y = __uint_as_float(o[4 * i + 1]) * wb;
+              v.z = __uint_as_float(o[4 * i + 2]) * wb;
+              v.w = __uint_as_float(o[4 * i + 3]) * wb;
+              if (read_old) {
+                const float4 u = dst[i];
+                v.x = fmaf(wa, u.x, v.x);
+                v.y = fmaf(wa, u.y, v.y);
+                v.z = fmaf(wa, u.z, v.z);
+                v.w = fmaf(wa, u.w, v.w);
+              }
+              dst[i] = v;
+            }
+          }
+        }
+        if (write) *lse_ptr = lse_new;
+      }
+    }
+  }
+
+  __syncwarp();
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int D>
+cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
+                   int num_items, cudaStream_t stream) {
+  auto kern = ring_fwd_step_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmem);
+  if (e != cudaSuccess) return e;
+  const long long grid = (long long)num_items * p.Hq;
+  if (grid <= 0) return cudaSuccess;
+  kern<<<(unsigned)grid, 384, FwdCfg<D>::kSmem, stream>>>(tq, tk, tv, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                            const FwdParams& p, int num_items, cudaStream_t stream) {
+  if (head_dim == 128) return launch<128>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 64) return launch<64>(tq, tk, tv, p, num_items, stream);
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace ra

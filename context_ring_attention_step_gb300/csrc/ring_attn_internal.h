@@ -1,0 +1,74 @@
+// ring_attn_internal.h -- work-item layouts shared by the host planner and the
+// kernels, and the kernel launch wrappers.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ra {
+
+// Forward work item: one CTA = up to 256 query rows (two 128-row tiles) of one
+// query chunk, all in one document, against up to two key ranges of the
+// key/value shard that the query shard holds at this ring step.  Ranges are
+// global token positions, sorted, disjoint, already clipped to the keys the
+// rows may see (for causal: keys < q1).  Grid: items x Hq.
+struct FwdItem {
+  int32_t q0, q1;    // query rows [q0, q1), q1 - q0 <= 256
+  int32_t kb0, ke0;  // key range 0 (may be empty)
+  int32_t kb1, ke1;  // key range 1 (may be empty)
+  int32_t flags;     // kFirstStep: write the running state instead of merging
+  int32_t tiles;     // number of 128-key tiles (work estimate)
+};
+
+// Backward work item: one CTA = one 128-row key/value tile of one key/value
+// head, against up to two query ranges of the query shard that holds this
+// key/value shard at this ring step (for causal: queries >= k0).  The CTA
+// loops over the Hq/Hkv query heads of the group.  Grid: items x Hkv.
+struct BwdItem {
+  int32_t k0, k1;    // key rows [k0, k1), k1 - k0 <= 128
+  int32_t qb0, qe0;  // query range 0 (may be empty)
+  int32_t qb1, qe1;  // query range 1 (may be empty)
+  int32_t flags;
+  int32_t tiles;     // number of 128-query tiles (work estimate)
+};
+
+constexpr int32_t kFirstStep = 1;
+
+struct FwdParams {
+  const FwdItem* items;
+  int32_t Hq, Hkv, T, causal;
+  float scale_log2;  // softmax scale * log2(e)
+  float* o_run;      // fp32 [T, Hq, D] running (normalised) output
+  float* lse;        // fp32 [Hq, T] running log-sum-exp (natural log)
+  int* status;       // workspace status word
+};
+
+struct BwdParams {
+  const BwdItem* items;
+  int32_t Hq, Hkv, T, causal;
+  float scale_log2;    // softmax scale * log2(e)
+  float scale;         // softmax scale
+  const float* lse2;   // [Hq, T] LSE * log2(e)
+  const float* delta;  // [Hq, T] rowsum(dO * O)
+  float* dq_acc;       // fp32 [T, Hq, D], scaled dq accumulated with reductions
+  float* dk_acc;       // fp32 [T, Hkv, D]
+  float* dv_acc;       // fp32 [T, Hkv, D]
+  int* status;
+};
+
+// Kernel launch wrappers (return the launch error).
+cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const FwdParams& p, int num_items,
+                            cudaStream_t stream);
+cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
+                            int num_items, cudaStream_t stream);
+// o (bf16) = o_run (fp32), elementwise.
+cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
+// Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e).
+cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout, const float* lse,
+                                  float* delta, float* lse2, int T, int Hq, int D,
+                                  cudaStream_t stream);
+
+}  // namespace ra

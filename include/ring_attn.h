@@ -1,0 +1,224 @@
+/*
+ * ring_attn.h -- C ABI of the GB300 ring-attention library (libring_attn.so).
+ *
+ * What it computes
+ * ----------------
+ * Ring attention for context parallelism.  The sequence (one document, or a
+ * packed THD batch of documents described by cu_seqlens) is cut along the
+ * token dimension into cp_size shards per document; the query shard of rank r
+ * stays put while the key/value shards travel around a ring, and at every
+ * ring step the rank computes attention of its queries against the key/value
+ * shard it currently holds, merging the partial result into a running
+ * (O, LSE).  Sources:
+ *   - NVSHMEM/XLA page, "Paralelismo de contexto y atencion en anillo": each
+ *     device processes its local part of the sequence, exchanges KV with its
+ *     ring neighbours and computes attention incrementally as KV blocks
+ *     circulate, keeping mathematical equivalence with standard attention.
+ *   - Accelerate guide, "Detalhes tecnicos": Q, K, V sharded along the
+ *     sequence (parts of size D//N), per-shard attention attn(Q_i, K_j, V_j)
+ *     for every j, then a combine of the partials.
+ *   - Accelerate guide: attention without a mask or with a causal mask only.
+ *   - Dynamic-CP page, "Reprogramacion dinamica y empaquetado de datos": THD
+ *     packing with cu_seqlens; a cp_size per document (per micro-batch).
+ * On one GPU the ring is run as successive ring steps over key/value shards
+ * that already sit in this GPU's memory; there is no communication.
+ *
+ * Readings where the pages are silent (all documented in the design notes):
+ *   - combine = exact log-sum-exp merge of normalised partials;
+ *   - zigzag layout: 2*cp equal chunks per document (floor boundaries), rank r
+ *     holds chunks r and 2*cp-1-r; contiguous layout: cp floor-boundary parts;
+ *   - ring order: at step s rank r holds key/value shard (r - s) mod cp;
+ *   - masks on global positions: a query sees a key iff both are in the same
+ *     document and (not causal or key <= query);
+ *   - GQA: query head h reads key/value head h / (Hq / Hkv);
+ *   - LSE is the natural log of sum exp(scale * q.k), fp32, layout [Hq, T].
+ *
+ * Conventions
+ * -----------
+ * Tensors are dense, row-major THD in natural (global) token order:
+ *   q, o, dout, dq : [T, Hq, head_dim]     k, v, dk, dv : [T, Hkv, head_dim]
+ * bf16 unless a *_fp32 flag says fp32.  The layout only decides which token
+ * ranges meet at which ring step; no permutation of the tensors is needed.
+ * Every device pointer must be 16-byte aligned.  head_dim is 64 or 128.
+ *
+ * Ownership: the caller owns every device buffer, including the workspace.
+ * The plan is host memory only (it never touches the GPU).  ra_fwd/ra_bwd
+ * copy the plan's work lists into the workspace with cudaMemcpyAsync, enqueue
+ * kernels on `stream` (a cudaStream_t, NULL = legacy default stream) and
+ * return without synchronising; nothing is allocated on the device.
+ *
+ * Errors: every entry point validates its arguments on the host first and
+ * returns RA_ERR_INVALID_ARG / RA_ERR_UNSUPPORTED / RA_ERR_WORKSPACE before
+ * enqueuing anything; a CUDA launch or copy failure returns RA_ERR_CUDA.
+ * ra_last_error() returns a thread-local message for the last non-OK status.
+ * Kernels never trap: a pipeline wait that exceeds its time limit makes the
+ * kernel record a code in the workspace header and return early;
+ * ra_workspace_status() reads that code (RA_ERR_TIMEOUT).
+ */
+#ifndef RING_ATTN_H
+#define RING_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RA_OK = 0,
+  RA_ERR_INVALID_ARG = 1,
+  RA_ERR_UNSUPPORTED = 2,
+  RA_ERR_CUDA = 3,
+  RA_ERR_WORKSPACE = 4,
+  RA_ERR_TIMEOUT = 5
+} ra_status;
+
+typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
+
+typedef struct ra_plan ra_plan; /* opaque, host memory only */
+
+/* Version of this ABI (bumped on any signature change). */
+int32_t ra_abi_version(void);
+
+/*
+ * Build a plan: shard every document, pair shards per ring step and cut the
+ * pairs into GPU work items.
+ *   cu_seqlens      host int32[num_docs + 1], cu_seqlens[0] == 0, non-decreasing;
+ *                   T = cu_seqlens[num_docs] (Dynamic-CP page, THD packing).
+ *   cp_size_per_doc host int32[num_docs] ring size of each document, or NULL to
+ *                   use cp_size for all (Dynamic-CP: cp chosen per micro-batch).
+ *   layout          RA_LAYOUT_CONTIGUOUS or RA_LAYOUT_ZIGZAG.
+ *   causal          1: key <= query within a document; 0: whole document.
+ *   num_q_heads, num_kv_heads: Hq % Hkv == 0.
+ *   softmax_scale   <= 0 selects 1/sqrt(head_dim).
+ * The plan copies what it needs; the caller's arrays may be freed afterwards.
+ */
+ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_docs,
+                         const int32_t* cp_size_per_doc, int32_t cp_size, int32_t layout,
+                         int32_t causal, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, float softmax_scale);
+
+/* Free a plan (NULL is ignored). */
+void ra_plan_destroy(ra_plan* plan);
+
+/*
+ * Workspace sizes in bytes for ra_fwd (given o_is_fp32) and ra_bwd (given
+ * grads_fp32).  Either output pointer may be NULL.
+ */
+ra_status ra_plan_workspace_bytes(const ra_plan* plan, int32_t o_is_fp32, int32_t grads_fp32,
+                                  size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * Plan statistics: number of ring steps (max cp over documents), visible
+ * (query, key) pairs summed over documents (per head), and the number of
+ * forward / backward work items over all steps.  Any pointer may be NULL.
+ */
+ra_status ra_plan_stats(const ra_plan* plan, int32_t* num_steps, int64_t* visible_pairs,
+                        int64_t* fwd_items, int64_t* bwd_items);
+
+/*
+ * Copy the plan's GPU work items to host memory, for inspection and tests.
+ * which = 0: forward items {q0, q1, kb0, ke0, kb1, ke1, flags, tiles};
+ * which = 1: backward items {k0, k1, qb0, qe0, qb1, qe1, flags, tiles}
+ * (8 int32 each, global token positions, ranges end-exclusive).
+ * items: host int32[8 * capacity] or NULL; step_offsets: host
+ * int64[num_steps + 1] or NULL (items of step s are [off[s], off[s+1])).
+ * *count receives the total number of items; RA_ERR_INVALID_ARG if
+ * capacity is too small for a non-NULL `items`.
+ */
+ra_status ra_plan_work_items(const ra_plan* plan, int32_t which, int32_t* items, int64_t capacity,
+                             int64_t* step_offsets, int64_t* count);
+
+/*
+ * Token ranges of shard `rank` of document `doc` (global positions, end
+ * exclusive): up to two ranges (zigzag: chunk rank and chunk 2*cp-1-rank).
+ * begin2/end2 are host int32[2]; *count receives 1 or 2 (empty ranges are
+ * still reported, with begin == end).  Accelerate guide, "Detalhes tecnicos".
+ */
+ra_status ra_shard_token_ranges(const ra_plan* plan, int32_t doc, int32_t rank,
+                                int32_t* begin2, int32_t* end2, int32_t* count);
+
+/*
+ * Forward: for s = 0 .. steps-1 every query shard r attends to key/value
+ * shard (r - s) mod cp of its document (one kernel launch per ring step,
+ * tcgen05 tensor-core block attention with online softmax); each step's
+ * partial (O_s, LSE_s) is merged exactly into the running (O, LSE) in the
+ * step kernel's epilogue.
+ *   q [T,Hq,d] bf16, k/v [T,Hkv,d] bf16 (device).
+ *   o [T,Hq,d]: bf16, or fp32 when o_is_fp32 != 0 (device, written).
+ *   lse [Hq,T] fp32 natural-log log-sum-exp (device, written).
+ *   workspace: device, >= ra_plan_workspace_bytes(.., o_is_fp32, ..).fwd.
+ */
+ra_status ra_fwd(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
+                 int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                 void* stream);
+
+/*
+ * Backward from the saved LSE: Delta = rowsum(dout * o) (o as returned by
+ * ra_fwd, dtype per o_is_fp32), then per ring step the probabilities are
+ * recomputed as P = exp(scale q.k - LSE) and
+ *   dV += P^T dO,  dS = P * (dO V^T - Delta),  dK += scale dS^T Q,  dQ += scale dS K,
+ * with dK/dV summed over the query heads of each GQA group.
+ *   dq [T,Hq,d], dk/dv [T,Hkv,d]: bf16, or fp32 when grads_fp32 != 0 (device, written).
+ *   workspace: device, >= ra_plan_workspace_bytes(.., grads_fp32).bwd.
+ */
+ra_status ra_bwd(const ra_plan* plan, const void* q, const void* k, const void* v,
+                 const void* o, int32_t o_is_fp32, const void* dout, const float* lse,
+                 void* dq, void* dk, void* dv, int32_t grads_fp32, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
+ * The ring step as its own call.  ra_fwd is exactly
+ *   ra_fwd_prepare; ra_fwd_ring_step(s) for s = 0 .. steps-1; ra_fwd_finish
+ * and ra_bwd is
+ *   ra_bwd_prepare; ra_bwd_ring_step(s) for every s; ra_bwd_finish
+ * on one workspace.  A multi-GPU driver would call the ring step after each
+ * key/value exchange (NVSHMEM/XLA page, "Patrones de comunicacion en la
+ * atencion en anillo": compute on the current KV block while the next one
+ * is fetched).  Each ring-step call enqueues exactly one kernel.
+ *
+ * ra_fwd_prepare: reset the status word and copy the forward work list.
+ * ra_fwd_ring_step: step in [0, steps); forward steps must run in order
+ *   (step 0 initialises the running (O, LSE), later steps merge into it).
+ * ra_fwd_finish: write the bf16 output from the fp32 running output (no-op
+ *   when o_is_fp32).
+ * ra_bwd_prepare: reset the status word, copy the backward work list,
+ *   compute Delta = rowsum(dout * o) and LSE in log2 units, zero the fp32
+ *   gradient accumulators (the gradients themselves when grads_fp32).
+ *   dq/dk/dv may be NULL unless grads_fp32.
+ * ra_bwd_ring_step: step in [0, steps), any order (accumulation only).
+ * ra_bwd_finish: cast the fp32 accumulators to the bf16 gradients (no-op
+ *   when grads_fp32).
+ */
+ra_status ra_fwd_prepare(const ra_plan* plan, int32_t o_is_fp32, void* workspace, size_t workspace_bytes,
+                         void* stream);
+ra_status ra_fwd_ring_step(const ra_plan* plan, int32_t step, const void* q, const void* k, const void* v,
+                           void* o, int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                           void* stream);
+ra_status ra_fwd_finish(const ra_plan* plan, void* o, int32_t o_is_fp32, void* workspace,
+                        size_t workspace_bytes, void* stream);
+ra_status ra_bwd_prepare(const ra_plan* plan, const void* o, int32_t o_is_fp32, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                         void* workspace, size_t workspace_bytes, void* stream);
+ra_status ra_bwd_ring_step(const ra_plan* plan, int32_t step, const void* q, const void* k, const void* v,
+                           const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                           void* workspace, size_t workspace_bytes, void* stream);
+ra_status ra_bwd_finish(const ra_plan* plan, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                        void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * Synchronise `stream` and read the status word that the last ra_fwd/ra_bwd
+ * call on this workspace left in its header: RA_OK, or RA_ERR_TIMEOUT if a
+ * kernel gave up on a pipeline wait (its outputs are then undefined).
+ */
+ra_status ra_workspace_status(const void* workspace, void* stream);
+
+/* Thread-local text for the last non-OK status returned on this thread. */
+const char* ra_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RING_ATTN_H */

@@ -146,3 +146,32 @@ def attention_rows(q, k, v, cu_seqlens, rows, head, causal=True, scale=None):
         lse[n] = m + np.log(np.exp(s - m).sum())
         o[n] = np.exp(s - lse[n]) @ v[b:kend, g, :]
     return o, lse
+
+
+def attention_rows_dq(q, k, v, do, cu_seqlens, rows, head, causal=True, scale=None):
+    """dq of single query rows of one head (exact, O(L d) per row).
+
+    Each row's softmax, its Delta = <dO_i, O_i> and its dq_i = scale sum_j
+    P_ij (<dO_i, v_j> - Delta_i) k_j need only that row.  Returns [len(rows), d].
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    T, Hq, d = q.shape
+    G = Hq // k.shape[1]
+    g = head // G
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    cu = np.asarray([int(c) for c in cu_seqlens])
+    dq = np.zeros((len(rows), d))
+    for n, i in enumerate(rows):
+        doc = int(np.searchsorted(cu, i, side="right") - 1)
+        b, e = int(cu[doc]), int(cu[doc + 1])
+        kend = i + 1 if causal else e
+        s = scale * (k[b:kend, g, :] @ q[i, head, :])
+        m = s.max()
+        p = np.exp(s - m)
+        p /= p.sum()
+        vb = v[b:kend, g, :]
+        o = p @ vb
+        dp = vb @ do[i, head, :]
+        ds = p * (dp - do[i, head, :] @ o)
+        dq[n] = scale * (ds @ k[b:kend, g, :])
+    return dq

@@ -1,0 +1,187 @@
+"""Host-side checks of the C-ABI library (no GPU): exports, planner, errors.
+
+The planner is checked against the oracle's own restatement of the layouts
+(``oracle.ring``), and its work items are expanded pair by pair to show that
+every visible (query, key) pair is covered exactly once, at the ring step the
+pairing rule assigns to it.
+"""
+
+import ctypes
+import re
+
+import pytest
+
+from oracle import ring as R
+from workloads import custom, workload
+
+HEADER = "include/ring_attn.h"
+
+
+def _declared():
+    import os
+    here = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    text = open(os.path.join(here, HEADER)).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ra_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol(lib_path):
+    lib = ctypes.CDLL(lib_path)
+    names = _declared()
+    assert len(names) >= 10
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+@pytest.fixture(scope="module")
+def ra(lib_path):
+    import context_ring_attention_step_gb300 as m
+    m.load_library(lib_path)
+    return m
+
+
+def test_abi_version(ra):
+    assert ra.load_library().ra_abi_version() == 1
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("lengths,cp", [([512], 4), ([10], 3), ([37, 3, 100], 5), ([1, 2, 7], 8)])
+def test_shard_ranges_match_oracle_layout(ra, layout, lengths, cp):
+    wl = custom(lengths, 2, 1, 64, cp, layout)
+    plan = ra.Plan(wl.cu_seqlens, cp, layout, True, 2, 1, 64)
+    for d, L in enumerate(lengths):
+        base = wl.cu_seqlens[d]
+        for r in range(cp):
+            want = [(base + a, base + b) for a, b in R.shard_ranges(L, cp, layout, r)]
+            assert plan.shard_token_ranges(d, r) == want
+
+
+def _expand_fwd(items, off, causal):
+    """{step: set of (q, k)} covered by forward items, with the causal mask applied."""
+    cover = {}
+    for s in range(len(off) - 1):
+        pairs = []
+        for it in items[off[s]:off[s + 1]]:
+            q0, q1, kb0, ke0, kb1, ke1, flags, tiles = it
+            assert q1 - q0 <= 256 and q1 > q0
+            assert (flags == 1) == (s == 0)
+            assert kb0 < ke0 and (kb1 == ke1 == 0 or ke0 <= kb1 < ke1)
+            for q in range(q0, q1):
+                for kb, ke in ((kb0, ke0), (kb1, ke1)):
+                    for k in range(kb, ke):
+                        if not causal or k <= q:
+                            pairs.append((q, k))
+        cover[s] = pairs
+    return cover
+
+
+def _expand_bwd(items, off, causal):
+    cover = {}
+    for s in range(len(off) - 1):
+        pairs = []
+        for it in items[off[s]:off[s + 1]]:
+            k0, k1, qb0, qe0, qb1, qe1, flags, tiles = it
+            assert k1 - k0 <= 128 and k1 > k0
+            for k in range(k0, k1):
+                for qb, qe in ((qb0, qe0), (qb1, qe1)):
+                    for q in range(qb, qe):
+                        if not causal or k <= q:
+                            pairs.append((q, k))
+        cover[s] = pairs
+    return cover
+
+
+def _expected(wl, causal):
+    """{step: set of visible (q, k)} from the oracle's layout and ring rule."""
+    want = {}
+    for d in range(wl.num_docs):
+        base, L, cp = wl.cu_seqlens[d], wl.doc_lengths[d], wl.cp_per_doc[d]
+        for s in range(cp):
+            for r in range(cp):
+                j = R.ring_source(r, s, cp)
+                qs = [base + x for a, b in R.shard_ranges(L, cp, wl.layout, r) for x in range(a, b)]
+                ks = [base + x for a, b in R.shard_ranges(L, cp, wl.layout, j) for x in range(a, b)]
+                want.setdefault(s, set()).update((q, k) for q in qs for k in ks if not causal or k <= q)
+    return want
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("lengths,cp", [([512], 4), ([700, 3, 1, 260], [4, 2, 1, 3]), ([130, 9], 8)])
+def test_work_items_cover_each_visible_pair_once(ra, layout, causal, lengths, cp):
+    wl = custom(lengths, 2, 2, 64, cp, layout, causal)
+    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), layout, causal, 2, 2, 64)
+    want = _expected(wl, causal)
+    for which, expand in (("fwd", _expand_fwd), ("bwd", _expand_bwd)):
+        items, off = plan.work_items(which)
+        got = expand(items, off, causal)
+        total = 0
+        for s, pairs in got.items():
+            assert len(pairs) == len(set(pairs)), (which, s)
+            assert set(pairs) == want.get(s, set()), (which, s)
+            total += len(pairs)
+        assert total == plan.stats()["visible_pairs"]
+
+
+def test_first_step_writes_every_row(ra):
+    wl = custom([700, 3, 1, 260], 2, 2, 64, [4, 2, 1, 3], "zigzag")
+    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), "zigzag", True, 2, 2, 64)
+    items, off = plan.work_items("fwd")
+    rows = set()
+    for it in items[off[0]:off[1]]:
+        rows.update(range(it[0], it[1]))
+    assert rows == set(range(wl.T))
+
+
+def test_visible_pairs_of_workloads(ra):
+    for name in ("tiny", "llama3_8b_32k", "varlen_65k"):
+        wl = workload(name)
+        plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d)
+        want = sum(L * (L + 1) // 2 for L in wl.doc_lengths)
+        st = plan.stats()
+        assert st["visible_pairs"] == want
+        assert st["steps"] == max(wl.cp_per_doc)
+
+
+def test_workspace_bytes_grow_with_outputs(ra):
+    plan = ra.Plan([0, 4096], 4, "zigzag", True, 8, 2, 128)
+    f_bf16, b_bf16 = plan.workspace_bytes(False, False)
+    f_fp32, b_fp32 = plan.workspace_bytes(True, True)
+    assert f_bf16 - f_fp32 >= 4096 * 8 * 128 * 4
+    assert b_bf16 - b_fp32 >= 4096 * (8 + 2 + 2) * 128 * 4
+
+
+@pytest.mark.parametrize("kwargs,status", [
+    (dict(cu=[0, 10], cp=0), 1),
+    (dict(cu=[0, 10], cp=2, hq=3, hkv=2), 1),
+    (dict(cu=[0, 10], cp=2, d=96), 2),
+    (dict(cu=[1, 10], cp=2), 1),
+    (dict(cu=[0, 10, 5], cp=2), 1),
+    (dict(cu=[0, 0], cp=2), 1),
+    (dict(cu=[0, 10], cp=2, layout=7), 1),
+])
+def test_plan_rejects_bad_arguments(ra, kwargs, status):
+    with pytest.raises(ra.RingAttnError) as e:
+        ra.Plan(kwargs["cu"], kwargs["cp"], kwargs.get("layout", "zigzag"), True, kwargs.get("hq", 2),
+                kwargs.get("hkv", 1), kwargs.get("d", 64))
+    assert e.value.status == status
+    assert len(str(e.value)) > 20
+
+
+def test_fwd_rejects_bad_pointers_before_touching_the_gpu(ra):
+    lib = ra.load_library()
+    plan = ra.Plan([0, 256], 2, "zigzag", True, 2, 1, 64)
+    p = ctypes.c_void_p
+    # NULL tensor
+    st = lib.ra_fwd(plan.handle, p(0), p(16), p(32), p(48), 0, p(64), p(128), 1 << 30, p(0))
+    assert st == 1
+    # misaligned pointer
+    st = lib.ra_fwd(plan.handle, p(8), p(16), p(32), p(48), 0, p(64), p(128), 1 << 30, p(0))
+    assert st == 1
+    # workspace too small
+    st = lib.ra_fwd(plan.handle, p(16), p(32), p(48), p(64), 0, p(80), p(96), 16, p(0))
+    assert st == 4
+    assert b"workspace too small" in lib.ra_last_error()
+    st = lib.ra_bwd(plan.handle, p(16), p(32), p(48), p(64), 0, p(80), p(96), p(112), p(128), p(144), 0,
+                    p(160), 16, p(0))
+    assert st == 4

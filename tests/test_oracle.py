@@ -316,6 +316,20 @@ def test_rows_sampler_matches_full_oracle():
         assert np.abs(rl - lse[h, rows]).max() < 1e-13
 
 
+def test_rows_dq_matches_full_oracle():
+    lengths = [33, 20]
+    T, Hq, Hkv, d = sum(lengths), 4, 2, 8
+    q, k, v, do = (_rand((T, Hq, d), 37), _rand((T, Hkv, d), 38),
+                   _rand((T, Hkv, d), 39), _rand((T, Hq, d), 40))
+    cu = _cu(lengths)
+    for causal in (True, False):
+        dq, _, _, _, _ = A.attention_bwd(q, k, v, do, cu, causal=causal, scale=0.3)
+        rows = [0, 5, 32, 33, 52]
+        for h in range(Hq):
+            rdq = A.attention_rows_dq(q, k, v, do, cu, rows, h, causal=causal, scale=0.3)
+            assert np.abs(rdq - dq[rows, h]).max() < 1e-12
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def test_pins_catch_a_planted_mask_slip(monkeypatch):
