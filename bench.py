@@ -21,7 +21,6 @@ from __future__ import annotations
 
 import argparse
 import json
-import math
 import os
 import statistics
 import subprocess
@@ -52,6 +51,21 @@ def peaks():
         return float(m["bf16_tflops"]), float(m["bf16_tflops_sustained"]), float(m["hbm_gbs"]), "measured"
     except Exception:
         return 1900.0, 1700.0, 6800.0, "fallback"
+
+
+def max_over_ranks(ms, dist=None, device=None):
+    """Max of a per-rank time over all ranks (identity on one process)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(ms)
+    import torch
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(world, flops_per_step, steps, ms_total):
+    """Whole-job throughput: every replica's useful FLOPs over the slowest rank's time."""
+    return world * flops_per_step * steps / (ms_total * 1e-3) / 1e12
 
 
 def step_pairs_bwd(items, off, causal):
@@ -319,18 +333,15 @@ def main():
                 t_f[s] += ev_f[s][0].elapsed_time(ev_f[s][1])
             if boff[s + 1] > boff[s]:
                 t_b[s] += ev_b[s][0].elapsed_time(ev_b[s][1])
-    ms_total = e0.elapsed_time(e1)
+    ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     if world > 1:
-        t = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
         dist.barrier()
     chk(lib.ra_workspace_status(P_(ws_f), sp))
     chk(lib.ra_workspace_status(P_(ws_b), sp))
 
     ff, fb = useful_flops(wl)
     ms_step = ms_total / args.steps
-    value = world * (ff + fb) * args.steps / (ms_total * 1e-3) / 1e12
+    value = whole_job_tflops(world, ff + fb, args.steps, ms_total)
     peak_b, peak_s, hbm, peak_kind = peaks()
     fwd_ms = sum(t_f) / args.steps
     bwd_ms = sum(t_b) / args.steps
@@ -374,12 +385,8 @@ def main():
                 dst.copy_(src, non_blocking=True)
         a1.record(stream)
         torch.cuda.synchronize()
-        e_ms = a0.elapsed_time(a1)
-        if world > 1:
-            t = torch.tensor([e_ms], device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_ms = float(t.item())
-        e2e = {"value": world * (ff + fb) * args.e2e_steps / (e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+        e_ms = max_over_ranks(a0.elapsed_time(a1), dist, dev)
+        e2e = {"value": whole_job_tflops(world, ff + fb, args.e2e_steps, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e_ms / args.e2e_steps}
 

@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(384, 1)
     const int row0 = it.q0 + 128 * qt;
     const int row = row0 + tid;
     const float sl2 = p.scale_log2;
-    float m_ref = kNegInf, l_sum = 0.f;
+    float m_ref = kNegInf, l_sum = 0.f, l_rnd = 0.f;
     uint32_t sph = 0;
     bool ok = true;
     const int na = qt == 0 ? n_act[0] : n_act[1];
@@ -269,10 +269,13 @@ __global__ void __launch_bounds__(384, 1)
         const float m_int = ceilf(m_new);
         alpha = ex2_approx(m_ref - m_int);
         l_sum *= alpha;
+        l_rnd *= alpha;
         m_ref = m_int;
       }
       const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
-      float ls0 = 0.f, ls1 = 0.f;
+      // Two row sums: of P (for the LSE) and of the bf16-rounded P that the PV MMA
+      // consumes (to normalise O, so O stays an exact convex combination of V).
+      float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t pk[16];
@@ -283,10 +286,13 @@ __global__ void __launch_bounds__(384, 1)
           ls0 += p0;
           ls1 += p1;
           pk[i] = pack_bf16x2(p0, p1);
+          lr0 += __uint_as_float(pk[i] << 16);
+          lr1 += __uint_as_float(pk[i] & 0xffff0000u);
         }
         tmem_st16(tS + 16 * c, pk);
       }
       l_sum += ls0 + ls1;
+      l_rnd += lr0 + lr1;
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1));
         // P is already stored, so the S registers are free here.
@@ -315,7 +321,7 @@ __global__ void __launch_bounds__(384, 1)
         const bool valid = row < it.q1;
         const bool first = (it.flags & kFirstStep) != 0;
         const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
-        const float inv_l = (l_sum > 0.f) ? 1.f / l_sum : 0.f;
+        const float inv_l = (l_rnd > 0.f) ? 1.f / l_rnd : 0.f;
         float* lse_ptr = p.lse + (size_t)h * p.T + row;
         float* orow = p.o_run + ((size_t)row * p.Hq + h) * D;
         const float lse_a = (valid && !first) ? *lse_ptr : kNegInf;
