@@ -74,7 +74,9 @@ def step_pairs_bwd(items, off, causal):
     out = []
     for s in range(len(off) - 1):
         tot = 0
-        for k0, k1, qb0, qe0, qb1, qe1, _, _ in items[off[s]:off[s + 1]]:
+        for k0, k1, qb0, qe0, qb1, qe1, flags, _ in items[off[s]:off[s + 1]]:
+            if flags >> 8:  # backward items are per key/value head: count head 0 only
+                continue
             keys = np.arange(k0, k1)
             for qb, qe in ((qb0, qe0), (qb1, qe1)):
                 if qe <= qb:

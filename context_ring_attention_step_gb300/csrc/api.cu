@@ -109,11 +109,15 @@ void build_items(ra_plan& P) {
             fs.push_back(it);
           }
         }
-        // ---- backward: key/value shard r is held by query shard (r + s) mod cp
+        // ---- backward: key/value shard r is held by query shard (r + s) mod cp.
+        // One item per (key tile, key/value head), grouped by shard pair and
+        // head: the CTAs running together then reduce into the dQ rows of one
+        // query shard and one GQA group, a working set that stays in L2.
         const int32_t qr = (r + s) % cp;
         int32_t kb2[2], ke2[2], qb2[2], qe2[2];
         const int nk2 = shard(L, cp, P.layout, r, kb2, ke2);
         const int nq2 = shard(L, cp, P.layout, qr, qb2, qe2);
+        for (int32_t g = 0; g < P.Hkv; ++g)
         for (int a = 0; a < nk2; ++a) {
           for (int32_t k0 = base + kb2[a]; k0 < base + ke2[a]; k0 += 128) {
             const int32_t k1 = std::min(k0 + 128, base + ke2[a]);
@@ -130,22 +134,25 @@ void build_items(ra_plan& P) {
             if (nr == 0) continue;
             it.qb0 = rb[0]; it.qe0 = re[0];
             it.qb1 = nr > 1 ? rb[1] : 0; it.qe1 = nr > 1 ? re[1] : 0;
-            it.flags = s == 0 ? ra::kFirstStep : 0;
+            it.flags = (s == 0 ? ra::kFirstStep : 0) | (g << ra::kHeadShift);
             it.tiles = tiles128(it.qb0, it.qe0) + tiles128(it.qb1, it.qe1);
             bs.push_back(it);
           }
         }
       }
     }
-    // longest items first, so the tail of each step launch is short
+    // forward: longest items first, so the tail of each step launch is short
     std::stable_sort(fs.begin(), fs.end(), [](const FwdItem& a, const FwdItem& b) { return a.tiles > b.tiles; });
-    std::stable_sort(bs.begin(), bs.end(), [](const BwdItem& a, const BwdItem& b) { return a.tiles > b.tiles; });
     P.fwd.insert(P.fwd.end(), fs.begin(), fs.end());
     P.bwd.insert(P.bwd.end(), bs.begin(), bs.end());
     P.fwd_off.push_back((int64_t)P.fwd.size());
     P.bwd_off.push_back((int64_t)P.bwd.size());
   }
 }
+
+// Row pitch (in floats) of the backward's per-head Delta and LSE*log2(e)
+// rows: T rounded up to 4, so every row starts 16-byte aligned for TMA.
+int64_t stat_pitch(const ra_plan& P) { return ((int64_t)P.T + 3) & ~int64_t(3); }
 
 struct FwdLayout {
   size_t items, orun, total;
@@ -171,9 +178,9 @@ BwdLayout bwd_layout(const ra_plan& P, int g_fp32) {
   l.items = off;
   off = align256(off + P.bwd.size() * sizeof(BwdItem));
   l.delta = off;
-  off = align256(off + (size_t)P.Hq * P.T * 4);
+  off = align256(off + (size_t)P.Hq * stat_pitch(P) * 4);
   l.lse2 = off;
-  off = align256(off + (size_t)P.Hq * P.T * 4);
+  off = align256(off + (size_t)P.Hq * stat_pitch(P) * 4);
   l.dq = l.dk = l.dv = 0;
   if (!g_fp32) {
     l.dq = off;
@@ -212,6 +219,19 @@ bool encode_thd(CUtensorMap* m, const void* base, int T, int H, int D) {
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Per-head fp32 rows [Hq, pitch] as a 2-D map {pitch, Hq}; box {128, 1}.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t pitch, int H) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)H};
+  cuuint64_t strides[1] = {(cuuint64_t)pitch * 4};
+  cuuint32_t box[2] = {128, 1};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -446,6 +466,7 @@ static ra::BwdParams bwd_params(const ra_plan* P, const BwdLayout& L, uint8_t* w
   p.scale_log2 = P->scale * 1.4426950408889634f;
   p.delta = reinterpret_cast<float*>(ws + L.delta);
   p.lse2 = reinterpret_cast<float*>(ws + L.lse2);
+  p.stat_pitch = stat_pitch(*P);
   p.dq_acc = grads_fp32 ? reinterpret_cast<float*>(dq) : reinterpret_cast<float*>(ws + L.dq);
   p.dk_acc = grads_fp32 ? reinterpret_cast<float*>(dk) : reinterpret_cast<float*>(ws + L.dk);
   p.dv_acc = grads_fp32 ? reinterpret_cast<float*>(dv) : reinterpret_cast<float*>(ws + L.dv);
@@ -473,8 +494,11 @@ ra_status ra_bwd_prepare(const ra_plan* P, const void* o, int32_t o_is_fp32, con
     if (e != cudaSuccess) return cuda_fail(e, "work-list copy");
   }
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
+  // the row padding past T is read by the tile loads (and masked): keep it finite
+  e = cudaMemsetAsync(ws + L.delta, 0, L.dq ? L.dq - L.delta : L.total - L.delta, st);
+  if (e != cudaSuccess) return cuda_fail(e, "stat reset");
   e = ra::launch_bwd_preprocess(o, o_is_fp32, dout, lse, const_cast<float*>(p.delta), const_cast<float*>(p.lse2),
-                                P->T, P->Hq, P->D, st);
+                                P->T, p.stat_pitch, P->Hq, P->D, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   const size_t nq = (size_t)P->T * P->Hq * P->D, nk = (size_t)P->T * P->Hkv * P->D;
   e = cudaMemsetAsync(p.dq_acc, 0, nq * 4, st);
@@ -498,14 +522,16 @@ ra_status ra_bwd_ring_step(const ra_plan* P, int32_t step, const void* q, const 
     return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
   const int64_t n = P->bwd_off[step + 1] - P->bwd_off[step];
   if (n == 0) return RA_OK;
-  CUtensorMap tq, tk, tv, tdo;
-  if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
-      !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D))
-    return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
   p.items = reinterpret_cast<const BwdItem*>(ws + L.items) + P->bwd_off[step];
-  cudaError_t e = ra::launch_bwd_step(P->D, tq, tk, tv, tdo, p, (int)n, reinterpret_cast<cudaStream_t>(stream_));
+  CUtensorMap tq, tk, tv, tdo, tl, td;
+  if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
+      !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D) ||
+      !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq) || !encode_rows(&td, p.delta, p.stat_pitch, P->Hq))
+    return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
+  cudaError_t e =
+      ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, p, (int)n, reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return cuda_fail(e, "backward step launch");
   return RA_OK;
 }

@@ -33,7 +33,7 @@ struct BwdCfg {
   static constexpr int kV = kTile;
   static constexpr int kStage0 = 2 * kTile;          // two stages of {Q, dO}
   static constexpr int kDS = kStage0 + 4 * kTile;    // dS^T, 128 x 128 bf16
-  static constexpr int kStat = kDS + 32768;          // per stage: lse2[128], delta[128]
+  static constexpr int kStat = kDS + 32768;          // per stage: lse2[128], delta[128] (TMA)
   static constexpr int kBar = kStat + 2 * 1024;
   static constexpr int kSmem = kBar + 256;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -42,14 +42,18 @@ struct BwdCfg {
   static constexpr uint32_t tdV = 0, tdK = D, tS = 2 * D, tP = 2 * D + 128;
 };
 
+// Query tiles of the CTA's pairs.  Tiles of a range start at the range start
+// rounded down to a multiple of 4, so the LSE/Delta slice of every tile is a
+// 16-byte aligned TMA load; columns before the range start are masked.
 struct PairList {
   int qb0, qe0, qb1, qe1, n0, nt, G, hbase;
   __device__ __forceinline__ int tile(int i) const { return i % nt; }
   __device__ __forceinline__ int head(int i) const { return hbase + i / nt; }
   __device__ __forceinline__ int start(int i) const {
     const int t = tile(i);
-    return t < n0 ? qb0 + 128 * t : qb1 + 128 * (t - n0);
+    return t < n0 ? (qb0 & ~3) + 128 * t : (qb1 & ~3) + 128 * (t - n0);
   }
+  __device__ __forceinline__ int lo(int i) const { return tile(i) < n0 ? qb0 : qb1; }
   __device__ __forceinline__ int end(int i) const { return tile(i) < n0 ? qe0 : qe1; }
 };
 
@@ -67,6 +71,7 @@ template <int D>
 __global__ void __launch_bounds__(384, 1)
     ring_bwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+                         const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
                          const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
@@ -92,12 +97,12 @@ __global__ void __launch_bounds__(384, 1)
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = blockIdx.x % p.Hkv;
-  const BwdItem it = p.items[blockIdx.x / p.Hkv];
+  const BwdItem it = p.items[blockIdx.x];
+  const int g = it.flags >> kHeadShift;
   PairList pl;
   pl.qb0 = it.qb0; pl.qe0 = it.qe0; pl.qb1 = it.qb1; pl.qe1 = it.qe1;
-  pl.n0 = ceil128(it.qb0, it.qe0);
-  pl.nt = pl.n0 + ceil128(it.qb1, it.qe1);
+  pl.n0 = ceil128(it.qb0 & ~3, it.qe0);
+  pl.nt = pl.n0 + ceil128(it.qb1 & ~3, it.qe1);
   pl.G = p.Hq / p.Hkv;
   pl.hbase = g * pl.G;
   const int npairs = pl.nt * pl.G;
@@ -126,44 +131,38 @@ __global__ void __launch_bounds__(384, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    bool ok = true;
-    int issued = 0;
     if (lane == 0) {
+      bool ok = true;
+      int issued = 0;
       tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmDO);
+      tma_prefetch_desc(&tmL); tma_prefetch_desc(&tmD);
       mbar_expect_tx(b_kv, 2 * C::kTile);
       for (int hf = 0; hf < D / 64; ++hf) {
         tma_load_3d(sK + hf * 16384, &tmK, b_kv, 64 * hf, g, it.k0);
         tma_load_3d(sV + hf * 16384, &tmV, b_kv, 64 * hf, g, it.k0);
       }
-    }
-    for (int i = 0; i < npairs; ++i) {
-      const int st = i & 1;
-      const uint32_t ph = (i >> 1) & 1;
-      if (!mbar_wait(b_empty + 8 * st, ph ^ 1, ab, 201)) { ok = false; break; }
-      // LSE (log2 units) and Delta of the 128 query columns of this pair
-      const int h = pl.head(i), q0 = pl.start(i), qe = pl.end(i);
-      float* sl = stat + st * 256;
-#pragma unroll
-      for (int c = lane; c < 128; c += 32) {
-        const int q = q0 + c;
-        const bool v = q < qe;
-        sl[c] = v ? p.lse2[(size_t)h * p.T + q] : __int_as_float(0x7f800000);
-        sl[128 + c] = v ? p.delta[(size_t)h * p.T + q] : 0.f;
-      }
-      __syncwarp();
-      if (lane == 0) {
-        mbar_expect_tx(b_full + 8 * st, 2 * C::kTile);
+      for (int i = 0; i < npairs; ++i) {
+        const int st = i & 1;
+        const uint32_t ph = (i >> 1) & 1;
+        if (!mbar_wait(b_empty + 8 * st, ph ^ 1, ab, 201)) { ok = false; break; }
+        const int h = pl.head(i), q0 = pl.start(i);
         const uint32_t sq = sSt + st * 2 * C::kTile, sdo = sq + C::kTile;
+        const uint32_t sl = smem_u32(stat + st * 256);
+        mbar_expect_tx(b_full + 8 * st, 2 * C::kTile + 2 * 512);
         for (int hf = 0; hf < D / 64; ++hf) {
           tma_load_3d(sq + hf * 16384, &tmQ, b_full + 8 * st, 64 * hf, h, q0);
           tma_load_3d(sdo + hf * 16384, &tmDO, b_full + 8 * st, 64 * hf, h, q0);
         }
+        // LSE (log2 units) and Delta of the tile's 128 query columns
+        tma_load_2d(sl, &tmL, b_full + 8 * st, q0, h);
+        tma_load_2d(sl + 512, &tmD, b_full + 8 * st, q0, h);
+        ++issued;
       }
-      ++issued;
-    }
-    if (!ok && lane == 0) {
-      mbar_wait_drain(b_kv, 0);
-      for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i) mbar_wait_drain(b_full + 8 * (i & 1), (i >> 1) & 1);
+      if (!ok) {
+        mbar_wait_drain(b_kv, 0);
+        for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
+          mbar_wait_drain(b_full + 8 * (i & 1), (i >> 1) & 1);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -231,13 +230,14 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < npairs; ++i) {
       const int st = i & 1;
       const uint32_t pi = i & 1;
-      const int q0 = pl.start(i), qe = pl.end(i);
-      const float* sl = stat + st * 256;
+      const int q0 = pl.start(i), qlo = pl.lo(i), qe = pl.end(i);
+      const float4* sl4 = reinterpret_cast<const float4*>(stat + st * 256);
       if (!mbar_wait(b_s, pi, ab, 210)) { ok = false; break; }
       tc_fence_after();
-      const bool need_mask = (it.k1 - it.k0 < 128) || (q0 + 128 > qe) || (p.causal && it.k1 - 1 > q0);
-      // visible query columns c satisfy  q0 + c < qe  and (causal) krow <= q0 + c
-      const int cmin = (krow >= it.k1) ? 128 : (p.causal ? max(0, krow - q0) : 0);
+      const bool need_mask =
+          (it.k1 - it.k0 < 128) || (q0 + 128 > qe) || (q0 < qlo) || (p.causal && it.k1 - 1 > q0);
+      // visible query columns c satisfy  qlo <= q0 + c < qe  and (causal) krow <= q0 + c
+      const int cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
       const int cmax = qe - q0;  // exclusive
       uint32_t pk[64];
 #pragma unroll
@@ -249,8 +249,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 32 * c + 2 * x;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * x]), sl2, -sl[c0]));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * x + 1]), sl2, -sl[c0 + 1]));
+          const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
+          const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * x]), sl2, -la));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * x + 1]), sl2, -lb));
           if (need_mask) {
             if (c0 < cmin || c0 >= cmax) p0 = 0.f;
             if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
@@ -280,8 +282,10 @@ __global__ void __launch_bounds__(384, 1)
         for (int x = 0; x < 16; ++x) {
           const int c0 = 32 * c + 2 * x;
           const uint32_t pp = pk[16 * c + x];
-          const float d0 = bf16lo(pp) * (__uint_as_float(r[2 * x]) - sl[128 + c0]) * scale;
-          const float d1 = bf16hi(pp) * (__uint_as_float(r[2 * x + 1]) - sl[128 + c0 + 1]) * scale;
+          const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
+          const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
+          const float d0 = bf16lo(pp) * (__uint_as_float(r[2 * x]) - da) * scale;
+          const float d1 = bf16hi(pp) * (__uint_as_float(r[2 * x + 1]) - db) * scale;
           w[x] = pack_bf16x2(d0, d1);
         }
         tmem_st16(tP + 16 * c, w);
@@ -345,7 +349,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(b_dqf);
       const int q = pl.start(i) + tid;
-      if (q < pl.end(i)) {
+      if (q >= pl.lo(i) && q < pl.end(i)) {
         float* dst = p.dq_acc + ((size_t)q * p.Hq + pl.head(i)) * D;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c)
@@ -368,22 +372,24 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                   const BwdParams& p, int num_items, cudaStream_t stream) {
+                   const CUtensorMap& tl, const CUtensorMap& td, const BwdParams& p, int num_items,
+                   cudaStream_t stream) {
   auto kern = ring_bwd_step_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
-  const long long grid = (long long)num_items * p.Hkv;
+  const long long grid = (long long)num_items;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, 384, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, p);
+  kern<<<(unsigned)grid, 384, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
-                            const CUtensorMap& tdo, const BwdParams& p, int num_items, cudaStream_t stream) {
-  if (head_dim == 128) return launch<128>(tq, tk, tv, tdo, p, num_items, stream);
-  if (head_dim == 64) return launch<64>(tq, tk, tv, tdo, p, num_items, stream);
+                            const CUtensorMap& tdo, const CUtensorMap& tl, const CUtensorMap& td,
+                            const BwdParams& p, int num_items, cudaStream_t stream) {
+  if (head_dim == 128) return launch<128>(tq, tk, tv, tdo, tl, td, p, num_items, stream);
+  if (head_dim == 64) return launch<64>(tq, tk, tv, tdo, tl, td, p, num_items, stream);
   return cudaErrorInvalidValue;
 }
 

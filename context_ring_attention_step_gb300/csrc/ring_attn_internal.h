@@ -22,9 +22,10 @@ struct FwdItem {
 };
 
 // Backward work item: one CTA = one 128-row key/value tile of one key/value
-// head, against up to two query ranges of the query shard that holds this
-// key/value shard at this ring step (for causal: queries >= k0).  The CTA
-// loops over the Hq/Hkv query heads of the group.  Grid: items x Hkv.
+// head (flags >> kHeadShift), against up to two query ranges of the query
+// shard that holds this key/value shard at this ring step (for causal:
+// queries >= k0).  The CTA loops over the Hq/Hkv query heads of the group.
+// Grid: one CTA per item.
 struct BwdItem {
   int32_t k0, k1;    // key rows [k0, k1), k1 - k0 <= 128
   int32_t qb0, qe0;  // query range 0 (may be empty)
@@ -34,6 +35,7 @@ struct BwdItem {
 };
 
 constexpr int32_t kFirstStep = 1;
+constexpr int32_t kHeadShift = 8;  // backward items: key/value head in flags bits [8, 31)
 
 struct FwdParams {
   const FwdItem* items;
@@ -49,8 +51,9 @@ struct BwdParams {
   int32_t Hq, Hkv, T, causal;
   float scale_log2;    // softmax scale * log2(e)
   float scale;         // softmax scale
-  const float* lse2;   // [Hq, T] LSE * log2(e)
-  const float* delta;  // [Hq, T] rowsum(dO * O)
+  const float* lse2;   // [Hq, stat_pitch] LSE * log2(e)
+  const float* delta;  // [Hq, stat_pitch] rowsum(dO * O)
+  int64_t stat_pitch;  // T rounded up to a multiple of 4
   float* dq_acc;       // fp32 [T, Hq, D], scaled dq accumulated with reductions
   float* dk_acc;       // fp32 [T, Hkv, D]
   float* dv_acc;       // fp32 [T, Hkv, D]
@@ -62,13 +65,15 @@ cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorM
                             const CUtensorMap& tv, const FwdParams& p, int num_items,
                             cudaStream_t stream);
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
-                            const CUtensorMap& tv, const CUtensorMap& tdo, const BwdParams& p,
-                            int num_items, cudaStream_t stream);
+                            const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tlse2,
+                            const CUtensorMap& tdelta, const BwdParams& p, int num_items,
+                            cudaStream_t stream);
 // o (bf16) = o_run (fp32), elementwise.
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
-// Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e).
+// Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e);
+// both written with row pitch `pitch` (>= T).
 cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout, const float* lse,
-                                  float* delta, float* lse2, int T, int Hq, int D,
+                                  float* delta, float* lse2, int T, int64_t pitch, int Hq, int D,
                                   cudaStream_t stream);
 
 }  // namespace ra

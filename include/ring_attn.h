@@ -112,7 +112,8 @@ ra_status ra_plan_workspace_bytes(const ra_plan* plan, int32_t o_is_fp32, int32_
 /*
  * Plan statistics: number of ring steps (max cp over documents), visible
  * (query, key) pairs summed over documents (per head), and the number of
- * forward / backward work items over all steps.  Any pointer may be NULL.
+ * forward / backward work items over all steps (backward items are per
+ * key/value head).  Any pointer may be NULL.
  */
 ra_status ra_plan_stats(const ra_plan* plan, int32_t* num_steps, int64_t* visible_pairs,
                         int64_t* fwd_items, int64_t* bwd_items);
@@ -121,7 +122,9 @@ ra_status ra_plan_stats(const ra_plan* plan, int32_t* num_steps, int64_t* visibl
  * Copy the plan's GPU work items to host memory, for inspection and tests.
  * which = 0: forward items {q0, q1, kb0, ke0, kb1, ke1, flags, tiles};
  * which = 1: backward items {k0, k1, qb0, qe0, qb1, qe1, flags, tiles}
- * (8 int32 each, global token positions, ranges end-exclusive).
+ * (8 int32 each, global token positions, ranges end-exclusive).  Forward
+ * items cover all query heads; backward items are per key/value head, which
+ * is flags >> 8 (bit 0 of flags marks ring step 0).
  * items: host int32[8 * capacity] or NULL; step_offsets: host
  * int64[num_steps + 1] or NULL (items of step s are [off[s], off[s+1])).
  * *count receives the total number of items; RA_ERR_INVALID_ARG if

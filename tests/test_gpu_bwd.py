@@ -72,14 +72,29 @@ def test_varlen_docs_per_doc_cp(ra, d):
 
 
 def test_ring_equals_gpu_cp1_fp32(ra):
+    """Backward ring invariance: from the same saved (O, LSE), every ring layout equals cp_size = 1.
+
+    The forward of each layout reaches O and LSE equal only up to fp32 rounding
+    (its own invariance is tested in test_gpu_fwd); feeding the backward those
+    last-bit differences flips ties in the bf16 rounding of P and dS.  So the
+    layouts are compared on one shared (O, LSE), with fp32 gradients, at 1e-3.
+    """
     wl = custom([2048, 700], 8, 2, 128, 4, "zigzag", True, seed=23, name="ring_vs_cp1")
-    q, k, v, do = draw_qkvdo(wl)
-    g1 = _run(ra, wl, q, k, v, do, grads_fp32=True, cp=[1, 1], o_fp32=True)
+    q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
+    plan1 = ra.Plan(wl.cu_seqlens, [1, 1], "zigzag", True, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    o, lse = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, [1, 1], "zigzag", True, wl.softmax_scale, o_fp32=True,
+                              plan=plan1, check=True)
+    g1 = ra.ring_attn_bwd(q, k, v, o, do, lse, wl.cu_seqlens, [1, 1], "zigzag", True, wl.softmax_scale,
+                          grads_fp32=True, plan=plan1, check=True)
+    g1 = [x.cpu().numpy() for x in g1]
     for layout in ("zigzag", "contiguous"):
-        for cp in ([4, 4], [8, 3]):
-            g = _run(ra, wl, q, k, v, do, grads_fp32=True, cp=cp, layout=layout, o_fp32=True)
+        for cp in ([4, 4], [8, 3], [2, 7]):
+            plan = ra.Plan(wl.cu_seqlens, cp, layout, True, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+            g = ra.ring_attn_bwd(q, k, v, o, do, lse, wl.cu_seqlens, cp, layout, True, wl.softmax_scale,
+                                 grads_fp32=True, plan=plan, check=True)
             for name, x, ref in zip(("dq", "dk", "dv"), g, g1):
-                assert np.abs(x - ref).max() <= RING_TOL, (layout, cp, name, np.abs(x - ref).max())
+                err = np.abs(x.cpu().numpy() - ref).max()
+                assert err <= RING_TOL, (layout, cp, name, err)
 
 
 def test_llama_32k_sampled_rows_and_sum_identities(ra):

@@ -75,12 +75,16 @@ def _expand_fwd(items, off, causal):
     return cover
 
 
-def _expand_bwd(items, off, causal):
+def _expand_bwd(items, off, causal, head=0):
+    """Pairs covered by the backward items of one key/value head."""
     cover = {}
     for s in range(len(off) - 1):
         pairs = []
         for it in items[off[s]:off[s + 1]]:
             k0, k1, qb0, qe0, qb1, qe1, flags, tiles = it
+            assert (flags & 1) == (s == 0)
+            if flags >> 8 != head:
+                continue
             assert k1 - k0 <= 128 and k1 > k0
             for k in range(k0, k1):
                 for qb, qe in ((qb0, qe0), (qb1, qe1)):
@@ -112,7 +116,8 @@ def test_work_items_cover_each_visible_pair_once(ra, layout, causal, lengths, cp
     wl = custom(lengths, 2, 2, 64, cp, layout, causal)
     plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), layout, causal, 2, 2, 64)
     want = _expected(wl, causal)
-    for which, expand in (("fwd", _expand_fwd), ("bwd", _expand_bwd)):
+    expanders = [("fwd", _expand_fwd)] + [("bwd", lambda i, o, c, h=h: _expand_bwd(i, o, c, h)) for h in range(2)]
+    for which, expand in expanders:
         items, off = plan.work_items(which)
         got = expand(items, off, causal)
         total = 0
