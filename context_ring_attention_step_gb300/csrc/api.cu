@@ -243,6 +243,13 @@ ra_status cuda_fail(cudaError_t e, const char* what) {
 
 }  // namespace
 
+namespace ra {
+ra_status set_last_error(ra_status st, const char* msg) {
+  g_err = msg;
+  return st;
+}
+}  // namespace ra
+
 extern "C" {
 
 int32_t ra_abi_version(void) { return 1; }

@@ -6,6 +6,8 @@
 #include <cuda_runtime.h>
 #include <cstdint>
 
+#include "../../include/ring_attn.h"
+
 namespace ra {
 
 // Forward work item: one CTA = up to 256 query rows (two 128-row tiles) of one
@@ -59,6 +61,9 @@ struct BwdParams {
   float* dv_acc;       // fp32 [T, Hkv, D]
   int* status;
 };
+
+// Record `msg` as this thread's last error text and return `st`.
+ra_status set_last_error(ra_status st, const char* msg);
 
 // Kernel launch wrappers (return the launch error).
 cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,

@@ -217,6 +217,29 @@ ra_status ra_bwd_finish(const ra_plan* plan, void* dq, void* dk, void* dv, int32
  */
 ra_status ra_workspace_status(const void* workspace, void* stream);
 
+/*
+ * Forward without any device allocation, for callers that cannot call
+ * cudaMalloc or hand out a workspace: plugins whose host framework owns all
+ * device memory and passes in only inputs and outputs, or serving loops that
+ * must not allocate (an allocation can synchronise the device or overrun a
+ * fixed memory budget).  (No counterpart on the pages; a library convenience.)
+ * Same computation and arguments as ra_fwd, minus the workspace: the
+ * workspace is a fixed 32 MiB device array inside this library, held on
+ * every GPU that loads it until the process exits.
+ *   - A plan whose forward workspace exceeds 32 MiB is rejected with
+ *     RA_ERR_WORKSPACE (ra_plan_workspace_bytes gives the need; o_is_fp32 = 1
+ *     removes the fp32 running output from it).
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array: calls that may overlap on the GPU (other
+ *     streams, other host threads) race and must be serialised by the caller.
+ *   - A kernel timeout is recorded in the array, which ra_workspace_status
+ *     cannot reach; validate outputs if that matters.
+ */
+ra_status ra_fwd_noalloc(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
+                         int32_t o_is_fp32, float* lse, void* stream);
+
 /* Thread-local text for the last non-OK status returned on this thread. */
 const char* ra_last_error(void);
 
