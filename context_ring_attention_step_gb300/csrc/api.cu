@@ -235,6 +235,20 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t pitch, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 THD accumulator [T, H, D] as a 3-D map {D, H, T}; box {32, 1, 128}
+// (128 bytes x 128 rows), 128-byte swizzle: the target of dQ reductions.
+bool encode_acc(CUtensorMap* m, const void* base, int T, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
+  cuuint32_t box[3] = {32, 1, 128};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 ra_status cuda_fail(cudaError_t e, const char* what) {
@@ -532,13 +546,14 @@ ra_status ra_bwd_ring_step(const ra_plan* P, int32_t step, const void* q, const 
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
   p.items = reinterpret_cast<const BwdItem*>(ws + L.items) + P->bwd_off[step];
-  CUtensorMap tq, tk, tv, tdo, tl, td;
+  CUtensorMap tq, tk, tv, tdo, tl, td, tdq;
   if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
       !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D) ||
-      !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq) || !encode_rows(&td, p.delta, p.stat_pitch, P->Hq))
+      !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq) || !encode_rows(&td, p.delta, p.stat_pitch, P->Hq) ||
+      !encode_acc(&tdq, p.dq_acc, P->T, P->Hq, P->D))
     return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
-  cudaError_t e =
-      ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, p, (int)n, reinterpret_cast<cudaStream_t>(stream_));
+  cudaError_t e = ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
+                                      reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return cuda_fail(e, "backward step launch");
   return RA_OK;
 }

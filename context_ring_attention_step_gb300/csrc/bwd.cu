@@ -8,17 +8,19 @@
 //   dS^T = scale P^T (dP^T - Delta),
 //   dV += P^T dO,  dK += dS^T Q,  dQ += dS K,
 // keeping dV and dK in tensor memory for the whole CTA and adding dQ into an
-// fp32 accumulator with vector reductions.
+// fp32 accumulator with TMA bulk tensor reductions.
 //
 // Warp roles (384 threads):
 //   warp 0      producer: K, V once; then Q_i, dO_i (TMA) and the LSE/Delta
 //               slices of each pair into a two-stage ring
 //   warp 1      TMEM owner + single-thread UMMA issuer
-//   warps 4-7   P / dS warpgroup, TMEM lanes = key rows; final dK/dV flush
-//   warps 8-11  dQ warpgroup, TMEM lanes = query rows
+//   warps 4-11  two compute warpgroups, each on half of the 128 query columns
+//               (P^T, dS^T) and half of the head dimension (dQ read-out and
+//               bulk reduction, final dK/dV flush)
 // Tensor memory: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T/dQ after.
-// P^T and dS^T (bf16) overwrite the first 64 columns of S^T and dP^T and feed
-// the dV and dK MMAs from tensor memory; dS^T is also written to shared memory
+// P^T and dS^T (bf16, two per column) overwrite columns [0,32) and [64,96) of
+// S^T and dP^T (each warpgroup packs into its own columns) and feed the dV and
+// dK MMAs from tensor memory; dS^T is also written to shared memory
 // (MN-major, 128-byte swizzle) as the A operand of the dQ MMA.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
@@ -72,7 +74,7 @@ __global__ void __launch_bounds__(384, 1)
     ring_bwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
-                         const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<D>;
   extern __shared__ __align__(1024) uint8_t smem[];
   if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
@@ -93,7 +95,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t b_dq = smem_u32(bars + 8);      // dQ_i in TMEM (and all earlier MMAs done)
   const uint32_t b_dqf = smem_u32(bars + 9);     // dQ_i read out (128 arrivals)
   const uint32_t b_drain = smem_u32(bars + 10);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  const uint32_t b_sf = smem_u32(bars + 11);     // [2] dQ staging written (128 arrivals per warpgroup)
+  const uint32_t b_se = smem_u32(bars + 13);     // [2] dQ staging read by the bulk reduction (1 arrival)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -112,10 +116,12 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(b_full, 1); mbar_init(b_full + 8, 1);
     mbar_init(b_empty, 1); mbar_init(b_empty + 8, 1);
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
-    mbar_init(b_pr, 128);
+    mbar_init(b_pr, 256);
     mbar_init(b_dq, 1);
-    mbar_init(b_dqf, 128);
+    mbar_init(b_dqf, 256);
     mbar_init(b_drain, 1);
+    mbar_init(b_sf, 128); mbar_init(b_sf + 8, 128);
+    mbar_init(b_se, 1); mbar_init(b_se + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -166,15 +172,12 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // Per pair i:  [dQ_{i-1} read out] dP_i | [P_i, dS_i written] dV_i, S_{i+1}, dK_i, dQ_i.
+    // S_{i+1} goes right after dV_i (the last reader of P_i in the S region), so
+    // the next pair's P phase overlaps dK_i and dQ_i.
     if (lane == 0) {
-      bool ok = mbar_wait(b_kv, 0, ab, 202);
-      for (int i = 0; i < npairs && ok; ++i) {
-        const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1, pi = i & 1;
-        const uint32_t sq = sSt + st * 2 * C::kTile, sdo = sq + C::kTile;
-        if (!mbar_wait(b_full + 8 * st, ph, ab, 203)) { ok = false; break; }
-        tc_fence_after();
-        // S^T = K Q^T
+      auto issue_s = [&](int i) {  // S^T_i = K Q_i^T
+        const uint32_t sq = sSt + (i & 1) * 2 * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -182,6 +185,19 @@ __global__ void __launch_bounds__(384, 1)
                   kk > 0);
         }
         umma_commit(b_s);
+      };
+      bool ok = mbar_wait(b_kv, 0, ab, 202);
+      if (ok && npairs > 0) {
+        ok = mbar_wait(b_full, 0, ab, 203);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+        }
+      }
+      for (int i = 0; i < npairs && ok; ++i) {
+        const int st = i & 1;
+        const uint32_t pi = i & 1;
+        const uint32_t sq = sSt + st * 2 * C::kTile, sdo = sq + C::kTile;
         // dP^T = V dO^T, once dQ_{i-1} has left this tensor-memory region
         if (i > 0) {
           if (!mbar_wait(b_dqf, pi ^ 1, ab, 204)) { ok = false; break; }
@@ -196,15 +212,22 @@ __global__ void __launch_bounds__(384, 1)
         umma_commit(b_dp);
         if (!mbar_wait(b_pr, pi, ab, 205)) { ok = false; break; }
         tc_fence_after();
-        // dV += P^T dO ; dK += dS^T Q   (A from tensor memory, B MN-major)
+        // dV += P^T dO   (A from tensor memory: packed query columns 0-63 in
+        // columns [0,32) of the S region, 64-127 in columns [64,96); B MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::tdV, tmem + C::tS + kk * 8, sdesc_sw128(sdo + kk * 2048, 16384, 1024), C::kIdescG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8,
+                  sdesc_sw128(sdo + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+        if (i + 1 < npairs) {
+          if (!mbar_wait(b_full + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(i + 1);
+        }
+        // dK += dS^T Q
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::tdK, tmem + C::tP + kk * 8, sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG,
-                  (i > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + C::tdK, tmem + C::tP + (kk >> 2) * 64 + (kk & 3) * 8,
+                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_empty + 8 * st);
         // dQ_i = dS K   (A = dS from shared memory, MN-major; B = K, MN-major)
 #pragma unroll
@@ -218,85 +241,145 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait_drain(b_drain, 0);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
-    // ------------------------------------------------------------ P / dS warpgroup
-    const int tid = threadIdx.x - 128;
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ compute warpgroups
+    // Two warpgroups split every 128-column tile: warpgroup w takes query
+    // columns [64w, 64w + 64) of S^T/dP^T, and head-dim columns [D/2 w, D/2 (w+1))
+    // of dQ, dK and dV.  TMEM lanes: key rows for S^T/dP^T/dK/dV, query rows for dQ.
+    const int wg = (warp - 4) >> 2;
+    const int tid = threadIdx.x - 128 * (1 + wg);
     const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
     const uint32_t tS = tmem_addr(tmem, lane_base, C::tS);
     const uint32_t tP = tmem_addr(tmem, lane_base, C::tP);
     const int krow = it.k0 + tid;
     const float sl2 = p.scale_log2, scale = p.scale;
+    constexpr int DH = D / 2;  // head-dim columns per warpgroup
     bool ok = true;
-    for (int i = 0; i < npairs; ++i) {
+    // dQ_j, this warpgroup's head-dim half: read it out of tensor memory, stage
+    // it 32 columns at a time in the warpgroup's quarter of the dS buffer (free
+    // once the dQ_j MMA is done) and add it into the fp32 accumulator with bulk
+    // tensor reductions.  Rows outside the query range carry exact zeros (their
+    // dS columns are masked) and rows past T are clipped by the tensor map.
+    const uint32_t stage_buf = sDS + wg * 16384;
+    const uint32_t sf = b_sf + 8 * wg, se = b_se + 8 * wg;
+    const bool leader = tid == 0;
+    uint32_t rounds = 0;  // staging rounds done by this warpgroup (barrier phases)
+    auto dq_out = [&](int j) -> bool {
+      if (!mbar_wait(b_dq, j & 1, ab, 220)) return false;
+      tc_fence_after();
+      uint32_t r[DH / 32][32];
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) tmem_ld32(tP + wg * DH + 32 * c, r[c]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) reg_fence32(r[c]);
+      tc_fence_before();
+      mbar_arrive(b_dqf);
+      const uint32_t row = stage_buf + tid * 128;
+#pragma unroll
+      for (int c = 0; c < DH / 32; ++c) {
+#pragma unroll
+        for (int pc = 0; pc < 8; ++pc)
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((pc ^ (tid & 7)) << 4)),
+                       "r"(r[c][4 * pc]), "r"(r[c][4 * pc + 1]), "r"(r[c][4 * pc + 2]), "r"(r[c][4 * pc + 3])
+                       : "memory");
+        fence_proxy_async_smem();
+        mbar_arrive(sf);
+        if (leader) {
+          if (mbar_wait(sf, rounds & 1, ab, 221)) {
+            tma_reduce_add_3d(&tmDQ, stage_buf, wg * DH + 32 * c, pl.head(j), pl.start(j));
+            bulk_commit();
+            bulk_wait_read();
+          }
+          mbar_arrive(se);
+        }
+        // the box has been read: the buffer may be rewritten (next round, or the dS phase)
+        if (!mbar_wait(se, rounds & 1, ab, 222)) return false;
+        ++rounds;
+      }
+      return true;
+    };
+    for (int i = 0; i < npairs && ok; ++i) {
       const int st = i & 1;
       const uint32_t pi = i & 1;
       const int q0 = pl.start(i), qlo = pl.lo(i), qe = pl.end(i);
       const float4* sl4 = reinterpret_cast<const float4*>(stat + st * 256);
-      if (!mbar_wait(b_s, pi, ab, 210)) { ok = false; break; }
-      tc_fence_after();
       const bool need_mask =
           (it.k1 - it.k0 < 128) || (q0 + 128 > qe) || (q0 < qlo) || (p.causal && it.k1 - 1 > q0);
       // visible query columns c satisfy  qlo <= q0 + c < qe  and (causal) krow <= q0 + c
       const int cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
       const int cmax = qe - q0;  // exclusive
-      uint32_t pk[64];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tS + 32 * c, r);
+      // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64)
+      if (!mbar_wait(b_s, pi, ab, 210)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t pk[32];
+      {
+        uint32_t r[2][32];
+        tmem_ld32(tS + 64 * wg, r[0]);
+        tmem_ld32(tS + 64 * wg + 32, r[1]);
         tmem_ld_wait();
-        reg_fence32(r);
+        reg_fence32(r[0]);
+        reg_fence32(r[1]);
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int c0 = 32 * c + 2 * x;
-          const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
-          const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[2 * x]), sl2, -la));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[2 * x + 1]), sl2, -lb));
-          if (need_mask) {
-            if (c0 < cmin || c0 >= cmax) p0 = 0.f;
-            if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int x = 0; x < 16; ++x) {
+            const int c0 = 64 * wg + 32 * c + 2 * x;
+            const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
+            const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
+            float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x]), sl2, -la));
+            float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x + 1]), sl2, -lb));
+            if (need_mask) {
+              if (c0 < cmin || c0 >= cmax) p0 = 0.f;
+              if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
+            }
+            pk[16 * c + x] = pack_bf16x2(p0, p1);
           }
-          pk[16 * c + x] = pack_bf16x2(p0, p1);
         }
-        uint32_t w[16];
+        // packed P^T goes to the first half of this warpgroup's own 64 columns
+        // (never into the other warpgroup's columns, which it may not have read yet)
+        uint32_t w0[16], w1[16];
 #pragma unroll
-        for (int x = 0; x < 16; ++x) w[x] = pk[16 * c + x];
-        tmem_st16(tS + 16 * c, w);
+        for (int x = 0; x < 16; ++x) { w0[x] = pk[x]; w1[x] = pk[16 + x]; }
+        tmem_st16(tS + 64 * wg, w0);
+        tmem_st16(tS + 64 * wg + 16, w1);
       }
+      // ---- dQ of the previous pair (frees the dP region for dP^T_i)
+      if (i > 0 && !dq_out(i - 1)) { ok = false; break; }
+      // ---- dS^T = scale P^T (dP^T - Delta)
       if (!mbar_wait(b_dp, pi, ab, 211)) { ok = false; break; }
       tc_fence_after();
-      // dS^T goes to shared memory too: the dQ MMA of the previous pair must be done with it
-      if (i > 0) {
-        if (!mbar_wait(b_dq, pi ^ 1, ab, 212)) { ok = false; break; }
-      }
-      const uint32_t ds_row = sDS + tid * 128;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t r[32];
-        tmem_ld32(tP + 32 * c, r);
+      {
+        uint32_t r[2][32];
+        tmem_ld32(tP + 64 * wg, r[0]);
+        tmem_ld32(tP + 64 * wg + 32, r[1]);
         tmem_ld_wait();
-        reg_fence32(r);
-        uint32_t w[16];
+        reg_fence32(r[0]);
+        reg_fence32(r[1]);
+        // this warpgroup's 64 query columns are chunk `wg` of the MN-major dS tile
+        const uint32_t ds_row = sDS + wg * 16384 + tid * 128;
 #pragma unroll
-        for (int x = 0; x < 16; ++x) {
-          const int c0 = 32 * c + 2 * x;
-          const uint32_t pp = pk[16 * c + x];
-          const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
-          const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
-          const float d0 = bf16lo(pp) * (__uint_as_float(r[2 * x]) - da) * scale;
-          const float d1 = bf16hi(pp) * (__uint_as_float(r[2 * x + 1]) - db) * scale;
-          w[x] = pack_bf16x2(d0, d1);
-        }
-        tmem_st16(tP + 16 * c, w);
-        // 32 query columns = 4 pieces of 16 B in 64-column chunk (c >> 1), swizzled by key row
+        for (int c = 0; c < 2; ++c) {
+          uint32_t w[16];
 #pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const int piece = (c & 1) * 4 + pc;
-          const uint32_t addr = ds_row + (c >> 1) * 16384 + ((piece ^ (tid & 7)) << 4);
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * pc]), "r"(w[4 * pc + 1]),
-                       "r"(w[4 * pc + 2]), "r"(w[4 * pc + 3])
-                       : "memory");
+          for (int x = 0; x < 16; ++x) {
+            const int c0 = 64 * wg + 32 * c + 2 * x;
+            const uint32_t pp = pk[16 * c + x];
+            const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
+            const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
+            const float d0 = bf16lo(pp) * (__uint_as_float(r[c][2 * x]) - da) * scale;
+            const float d1 = bf16hi(pp) * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
+            w[x] = pack_bf16x2(d0, d1);
+          }
+          tmem_st16(tP + 64 * wg + 16 * c, w);
+#pragma unroll
+          for (int pc = 0; pc < 4; ++pc) {
+            const int piece = c * 4 + pc;
+            const uint32_t addr = ds_row + ((piece ^ (tid & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * pc]), "r"(w[4 * pc + 1]),
+                         "r"(w[4 * pc + 2]), "r"(w[4 * pc + 3])
+                         : "memory");
+          }
         }
       }
       tmem_st_wait();
@@ -304,59 +387,29 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(b_pr);
     }
+    if (ok && npairs > 0) ok = dq_out(npairs - 1);  // also: every MMA of the CTA is done
+    if (leader) bulk_wait_all();
     if (ok && npairs > 0) {
-      // all MMAs of the CTA are complete once the last dQ has landed
-      if (mbar_wait(b_dq, (npairs - 1) & 1, ab, 213)) {
-        tc_fence_after();
-        const bool valid = krow < it.k1;
-        float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D;
-        float* dk_row = p.dk_acc + ((size_t)krow * p.Hkv + g) * D;
+      const bool valid = krow < it.k1;
+      float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
+      float* dk_row = p.dk_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
 #pragma unroll
-        for (int which = 0; which < 2; ++which) {
-          const uint32_t t = tmem_addr(tmem, lane_base, which == 0 ? C::tdV : C::tdK);
-          float* dst = which == 0 ? dv_row : dk_row;
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t = tmem_addr(tmem, lane_base, (which == 0 ? C::tdV : C::tdK) + wg * DH);
+        float* dst = which == 0 ? dv_row : dk_row;
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(t + 32 * c, r);
-            tmem_ld_wait();
-            reg_fence32(r);
-            if (valid) {
+        for (int c = 0; c < DH / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t + 32 * c, r);
+          tmem_ld_wait();
+          reg_fence32(r);
+          if (valid) {
 #pragma unroll
-              for (int x = 0; x < 8; ++x)
-                red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                           __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
-            }
+            for (int x = 0; x < 8; ++x)
+              red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                         __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
           }
         }
-      }
-    }
-  } else if (warp >= 8) {
-    // ------------------------------------------------------------ dQ warpgroup
-    const int tid = threadIdx.x - 256;
-    const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
-    const uint32_t tQ = tmem_addr(tmem, lane_base, C::tP);
-    for (int i = 0; i < npairs; ++i) {
-      const uint32_t pi = i & 1;
-      if (!mbar_wait(b_dq, pi, ab, 220)) break;
-      tc_fence_after();
-      uint32_t r[D / 32][32];
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) tmem_ld32(tQ + 32 * c, r[c]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < D / 32; ++c) reg_fence32(r[c]);
-      tc_fence_before();
-      mbar_arrive(b_dqf);
-      const int q = pl.start(i) + tid;
-      if (q >= pl.lo(i) && q < pl.end(i)) {
-        float* dst = p.dq_acc + ((size_t)q * p.Hq + pl.head(i)) * D;
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c)
-#pragma unroll
-          for (int x = 0; x < 8; ++x)
-            red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[c][4 * x]), __uint_as_float(r[c][4 * x + 1]),
-                       __uint_as_float(r[c][4 * x + 2]), __uint_as_float(r[c][4 * x + 3]));
       }
     }
   }
@@ -372,14 +425,14 @@ __global__ void __launch_bounds__(384, 1)
 
 template <int D>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const CUtensorMap& tdo,
-                   const CUtensorMap& tl, const CUtensorMap& td, const BwdParams& p, int num_items,
-                   cudaStream_t stream) {
+                   const CUtensorMap& tl, const CUtensorMap& td, const CUtensorMap& tdq, const BwdParams& p,
+                   int num_items, cudaStream_t stream) {
   auto kern = ring_bwd_step_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, BwdCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, 384, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, p);
+  kern<<<(unsigned)grid, 384, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, p);
   return cudaGetLastError();
 }
 
@@ -387,9 +440,9 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const CUtensorMap& tdo, const CUtensorMap& tl, const CUtensorMap& td,
-                            const BwdParams& p, int num_items, cudaStream_t stream) {
-  if (head_dim == 128) return launch<128>(tq, tk, tv, tdo, tl, td, p, num_items, stream);
-  if (head_dim == 64) return launch<64>(tq, tk, tv, tdo, tl, td, p, num_items, stream);
+                            const CUtensorMap& tdq, const BwdParams& p, int num_items, cudaStream_t stream) {
+  if (head_dim == 128) return launch<128>(tq, tk, tv, tdo, tl, td, tdq, p, num_items, stream);
+  if (head_dim == 64) return launch<64>(tq, tk, tv, tdo, tl, td, tdq, p, num_items, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -116,6 +116,12 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, p.status};
 
+  // Register split: 384 threads x 168 at launch.  The producer/MMA warpgroup
+  // drops to 56 and the two softmax warpgroups rise to 216:
+  // 128 x 56 + 256 x 216 = 62464 <= 64512.  Each warpgroup sets its limit at
+  // the head of its own branch, so no code is shared across the two limits.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 56;");
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
@@ -216,7 +222,9 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait_drain(b_drain, 0);
       }
     }
-  } else if (warp >= 4) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
     // ------------------------------------------------------------ softmax
     const int qt = (warp - 4) >> 2;
     const int tid = threadIdx.x - 128 * (1 + qt);
@@ -252,11 +260,11 @@ __global__ void __launch_bounds__(384, 1)
       }
       float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        mx0 = fmaxf(mx0, __uint_as_float(r[0][c]));
-        mx1 = fmaxf(mx1, __uint_as_float(r[1][c]));
-        mx2 = fmaxf(mx2, __uint_as_float(r[2][c]));
-        mx3 = fmaxf(mx3, __uint_as_float(r[3][c]));
+      for (int c = 0; c < 32; c += 2) {
+        mx0 = fmax3(mx0, __uint_as_float(r[0][c]), __uint_as_float(r[0][c + 1]));
+        mx1 = fmax3(mx1, __uint_as_float(r[1][c]), __uint_as_float(r[1][c + 1]));
+        mx2 = fmax3(mx2, __uint_as_float(r[2][c]), __uint_as_float(r[2][c + 1]));
+        mx3 = fmax3(mx3, __uint_as_float(r[3][c]), __uint_as_float(r[3][c + 1]));
       }
       const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
       const float m_new = fmaxf(m_ref, m_tile);

@@ -56,7 +56,7 @@ struct BwdParams {
   const float* lse2;   // [Hq, stat_pitch] LSE * log2(e)
   const float* delta;  // [Hq, stat_pitch] rowsum(dO * O)
   int64_t stat_pitch;  // T rounded up to a multiple of 4
-  float* dq_acc;       // fp32 [T, Hq, D], scaled dq accumulated with reductions
+  float* dq_acc;       // fp32 [T, Hq, D], scaled dq accumulated with bulk reductions
   float* dk_acc;       // fp32 [T, Hkv, D]
   float* dv_acc;       // fp32 [T, Hkv, D]
   int* status;
@@ -71,8 +71,8 @@ cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorM
                             cudaStream_t stream);
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tlse2,
-                            const CUtensorMap& tdelta, const BwdParams& p, int num_items,
-                            cudaStream_t stream);
+                            const CUtensorMap& tdelta, const CUtensorMap& tdq_acc, const BwdParams& p,
+                            int num_items, cudaStream_t stream);
 // o (bf16) = o_run (fp32), elementwise.
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
 // Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e);
