@@ -95,9 +95,7 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t b_dq = smem_u32(bars + 8);      // dQ_i in TMEM (and all earlier MMAs done)
   const uint32_t b_dqf = smem_u32(bars + 9);     // dQ_i read out (128 arrivals)
   const uint32_t b_drain = smem_u32(bars + 10);
-  const uint32_t b_sf = smem_u32(bars + 11);     // [2] dQ staging written (128 arrivals per warpgroup)
-  const uint32_t b_se = smem_u32(bars + 13);     // [2] dQ staging read by the bulk reduction (1 arrival)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 15);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -120,8 +118,6 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(b_dq, 1);
     mbar_init(b_dqf, 256);
     mbar_init(b_drain, 1);
-    mbar_init(b_sf, 128); mbar_init(b_sf + 8, 128);
-    mbar_init(b_se, 1); mbar_init(b_se + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -255,17 +251,27 @@ __global__ void __launch_bounds__(384, 1)
     const float sl2 = p.scale_log2, scale = p.scale;
     constexpr int DH = D / 2;  // head-dim columns per warpgroup
     bool ok = true;
-    // dQ_j, this warpgroup's head-dim half: read it out of tensor memory, stage
-    // it 32 columns at a time in the warpgroup's quarter of the dS buffer (free
-    // once the dQ_j MMA is done) and add it into the fp32 accumulator with bulk
-    // tensor reductions.  Rows outside the query range carry exact zeros (their
-    // dS columns are masked) and rows past T are clipped by the tensor map.
-    const uint32_t stage_buf = sDS + wg * 16384;
-    const uint32_t sf = b_sf + 8 * wg, se = b_se + 8 * wg;
-    const bool leader = tid == 0;
-    uint32_t rounds = 0;  // staging rounds done by this warpgroup (barrier phases)
+    // dQ_j, this warpgroup's head-dim half: read out of tensor memory, staged
+    // 32 columns at a time and added into the fp32 accumulator by bulk tensor
+    // reductions.  Every thread stages only its own 128-byte row of the dS
+    // buffer (the same row it writes dS^T to), so each warp hands its 32 rows to
+    // the TMA on its own: no cross-warp synchronisation.  Rows outside the
+    // query range carry exact zeros (their dS columns are masked); rows past T
+    // are clipped by the tensor map.
+    const uint32_t row_addr = sDS + wg * 16384 + tid * 128;
+    const uint32_t warp_box = sDS + wg * 16384 + (tid & ~31) * 128;
+    const bool lead = lane == 0;
+    // all lanes of a warp take the same branch after a bounded wait
+    auto wait_warp = [&](uint32_t bar, uint32_t parity, int site) -> bool {
+      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, site)) != 0;
+    };
+    // the TMA must have read this warp's staged rows before they are rewritten
+    auto staging_free = [&]() {
+      if (lead) bulk_wait_read();
+      __syncwarp();
+    };
     auto dq_out = [&](int j) -> bool {
-      if (!mbar_wait(b_dq, j & 1, ab, 220)) return false;
+      if (!wait_warp(b_dq, j & 1, 220)) return false;
       tc_fence_after();
       uint32_t r[DH / 32][32];
 #pragma unroll
@@ -275,27 +281,20 @@ __global__ void __launch_bounds__(384, 1)
       for (int c = 0; c < DH / 32; ++c) reg_fence32(r[c]);
       tc_fence_before();
       mbar_arrive(b_dqf);
-      const uint32_t row = stage_buf + tid * 128;
 #pragma unroll
       for (int c = 0; c < DH / 32; ++c) {
+        staging_free();
 #pragma unroll
         for (int pc = 0; pc < 8; ++pc)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row + ((pc ^ (tid & 7)) << 4)),
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((pc ^ (tid & 7)) << 4)),
                        "r"(r[c][4 * pc]), "r"(r[c][4 * pc + 1]), "r"(r[c][4 * pc + 2]), "r"(r[c][4 * pc + 3])
                        : "memory");
         fence_proxy_async_smem();
-        mbar_arrive(sf);
-        if (leader) {
-          if (mbar_wait(sf, rounds & 1, ab, 221)) {
-            tma_reduce_add_3d(&tmDQ, stage_buf, wg * DH + 32 * c, pl.head(j), pl.start(j));
-            bulk_commit();
-            bulk_wait_read();
-          }
-          mbar_arrive(se);
+        __syncwarp();
+        if (lead) {
+          tma_reduce_add_3d(&tmDQ, warp_box, wg * DH + 32 * c, pl.head(j), pl.start(j) + (tid & ~31));
+          bulk_commit();
         }
-        // the box has been read: the buffer may be rewritten (next round, or the dS phase)
-        if (!mbar_wait(se, rounds & 1, ab, 222)) return false;
-        ++rounds;
       }
       return true;
     };
@@ -310,7 +309,7 @@ __global__ void __launch_bounds__(384, 1)
       const int cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
       const int cmax = qe - q0;  // exclusive
       // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64)
-      if (!mbar_wait(b_s, pi, ab, 210)) { ok = false; break; }
+      if (!wait_warp(b_s, pi, 210)) { ok = false; break; }
       tc_fence_after();
       uint32_t pk[32];
       {
@@ -347,7 +346,7 @@ __global__ void __launch_bounds__(384, 1)
       // ---- dQ of the previous pair (frees the dP region for dP^T_i)
       if (i > 0 && !dq_out(i - 1)) { ok = false; break; }
       // ---- dS^T = scale P^T (dP^T - Delta)
-      if (!mbar_wait(b_dp, pi, ab, 211)) { ok = false; break; }
+      if (!wait_warp(b_dp, pi, 211)) { ok = false; break; }
       tc_fence_after();
       {
         uint32_t r[2][32];
@@ -357,7 +356,8 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence32(r[0]);
         reg_fence32(r[1]);
         // this warpgroup's 64 query columns are chunk `wg` of the MN-major dS tile
-        const uint32_t ds_row = sDS + wg * 16384 + tid * 128;
+        const uint32_t ds_row = row_addr;
+        staging_free();
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
           uint32_t w[16];
@@ -388,7 +388,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_arrive(b_pr);
     }
     if (ok && npairs > 0) ok = dq_out(npairs - 1);  // also: every MMA of the CTA is done
-    if (leader) bulk_wait_all();
+    if (lead) bulk_wait_all();
     if (ok && npairs > 0) {
       const bool valid = krow < it.k1;
       float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
