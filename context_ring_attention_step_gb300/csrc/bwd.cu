@@ -252,23 +252,21 @@ __global__ void __launch_bounds__(384, 1)
     constexpr int DH = D / 2;  // head-dim columns per warpgroup
     bool ok = true;
     // dQ_j, this warpgroup's head-dim half: read out of tensor memory, staged
-    // 32 columns at a time and added into the fp32 accumulator by bulk tensor
-    // reductions.  Every thread stages only its own 128-byte row of the dS
-    // buffer (the same row it writes dS^T to), so each warp hands its 32 rows to
-    // the TMA on its own: no cross-warp synchronisation.  Rows outside the
+    // 16 columns at a time and added into the fp32 accumulator by bulk tensor
+    // reductions.  Each warp stages only its own 32 rows, in the 4 KB of the
+    // dS buffer that it also writes dS^T to, split into two 2 KB halves used
+    // alternately (64-byte swizzle): a round waits only for the reads of the
+    // round before last, and no warp waits for another.  Rows outside the
     // query range carry exact zeros (their dS columns are masked); rows past T
     // are clipped by the tensor map.
     const uint32_t row_addr = sDS + wg * 16384 + tid * 128;
     const uint32_t warp_box = sDS + wg * 16384 + (tid & ~31) * 128;
+    const uint32_t half_row = (uint32_t)lane * 64;
+    const uint32_t swz64 = (uint32_t)((lane >> 1) & 3);
     const bool lead = lane == 0;
     // all lanes of a warp take the same branch after a bounded wait
     auto wait_warp = [&](uint32_t bar, uint32_t parity, int site) -> bool {
       return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, site)) != 0;
-    };
-    // the TMA must have read this warp's staged rows before they are rewritten
-    auto staging_free = [&]() {
-      if (lead) bulk_wait_read();
-      __syncwarp();
     };
     auto dq_out = [&](int j) -> bool {
       if (!wait_warp(b_dq, j & 1, 220)) return false;
@@ -282,17 +280,21 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(b_dqf);
 #pragma unroll
-      for (int c = 0; c < DH / 32; ++c) {
-        staging_free();
+      for (int c = 0; c < DH / 16; ++c) {
+        const uint32_t buf = warp_box + (c & 1) * 2048;
+        if (lead) bulk_wait_read_all_but_one();  // this half's previous box has been read
+        __syncwarp();
 #pragma unroll
-        for (int pc = 0; pc < 8; ++pc)
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((pc ^ (tid & 7)) << 4)),
-                       "r"(r[c][4 * pc]), "r"(r[c][4 * pc + 1]), "r"(r[c][4 * pc + 2]), "r"(r[c][4 * pc + 3])
+        for (int pc = 0; pc < 4; ++pc) {
+          const int x = 16 * (c & 1) + 4 * pc;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + half_row + ((pc ^ swz64) << 4)),
+                       "r"(r[c >> 1][x]), "r"(r[c >> 1][x + 1]), "r"(r[c >> 1][x + 2]), "r"(r[c >> 1][x + 3])
                        : "memory");
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lead) {
-          tma_reduce_add_3d(&tmDQ, warp_box, wg * DH + 32 * c, pl.head(j), pl.start(j) + (tid & ~31));
+          tma_reduce_add_3d(&tmDQ, buf, wg * DH + 16 * c, pl.head(j), pl.start(j) + (tid & ~31));
           bulk_commit();
         }
       }
@@ -356,11 +358,9 @@ __global__ void __launch_bounds__(384, 1)
         reg_fence32(r[0]);
         reg_fence32(r[1]);
         // this warpgroup's 64 query columns are chunk `wg` of the MN-major dS tile
-        const uint32_t ds_row = row_addr;
-        staging_free();
+        uint32_t w[2][16];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
-          uint32_t w[16];
 #pragma unroll
           for (int x = 0; x < 16; ++x) {
             const int c0 = 64 * wg + 32 * c + 2 * x;
@@ -369,18 +369,22 @@ __global__ void __launch_bounds__(384, 1)
             const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
             const float d0 = bf16lo(pp) * (__uint_as_float(r[c][2 * x]) - da) * scale;
             const float d1 = bf16hi(pp) * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
-            w[x] = pack_bf16x2(d0, d1);
+            w[c][x] = pack_bf16x2(d0, d1);
           }
-          tmem_st16(tP + 64 * wg + 16 * c, w);
+          tmem_st16(tP + 64 * wg + 16 * c, w[c]);
+        }
+        // the TMA must have read this warp's staged dQ rows before they are rewritten
+        if (lead) bulk_wait_read();
+        __syncwarp();
+#pragma unroll
+        for (int c = 0; c < 2; ++c)
 #pragma unroll
           for (int pc = 0; pc < 4; ++pc) {
             const int piece = c * 4 + pc;
-            const uint32_t addr = ds_row + ((piece ^ (tid & 7)) << 4);
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(w[4 * pc]), "r"(w[4 * pc + 1]),
-                         "r"(w[4 * pc + 2]), "r"(w[4 * pc + 3])
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((piece ^ (tid & 7)) << 4)),
+                         "r"(w[c][4 * pc]), "r"(w[c][4 * pc + 1]), "r"(w[c][4 * pc + 2]), "r"(w[c][4 * pc + 3])
                          : "memory");
           }
-        }
       }
       tmem_st_wait();
       fence_proxy_async_smem();
