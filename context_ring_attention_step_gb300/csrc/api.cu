@@ -235,18 +235,18 @@ bool encode_rows(CUtensorMap* m, const void* base, int64_t pitch, int H) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 THD accumulator [T, H, D] as a 3-D map {D, H, T}; box {16, 1, 32}
-// (64 bytes x 32 rows, one warp's rows), 64-byte swizzle: the target of the
+// fp32 THD accumulator [T, H, D] as a 3-D map {D, H, T}; box {32, 1, 32}
+// (128 bytes x 32 rows, one warp's rows), 128-byte swizzle: the target of the
 // dQ reductions.
 bool encode_acc(CUtensorMap* m, const void* base, int T, int H, int D) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * 4, (cuuint64_t)H * D * 4};
-  cuuint32_t box[3] = {16, 1, 32};
+  cuuint32_t box[3] = {32, 1, 32};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

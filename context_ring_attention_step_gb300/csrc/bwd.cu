@@ -10,13 +10,15 @@
 // keeping dV and dK in tensor memory for the whole CTA and adding dQ into an
 // fp32 accumulator with TMA bulk tensor reductions.
 //
-// Warp roles (384 threads):
-//   warp 0      producer: K, V once; then Q_i, dO_i (TMA) and the LSE/Delta
-//               slices of each pair into a two-stage ring
-//   warp 1      TMEM owner + single-thread UMMA issuer
-//   warps 4-11  two compute warpgroups, each on half of the 128 query columns
-//               (P^T, dS^T) and half of the head dimension (dQ read-out and
-//               bulk reduction, final dK/dV flush)
+// Warp roles (512 threads):
+//   warp 0       producer: K, V once; then Q_i with its LSE/Delta slices into a
+//                two-stage ring, and dO_i into a single buffer
+//   warp 1       TMEM owner + single-thread UMMA issuer
+//   warps 4-11   two compute warpgroups, each on half of the 128 query columns
+//                (P^T, dS^T) and, at the end, half of the head dimension of dK/dV
+//   warps 12-15  dQ warpgroup: reads dQ_i out of tensor memory, stages it in its
+//                own shared-memory buffer and adds it into the accumulator with
+//                bulk reductions, off the compute warpgroups' path
 // Tensor memory: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T/dQ after.
 // P^T and dS^T (bf16, two per column) overwrite columns [0,32) and [64,96) of
 // S^T and dP^T (each warpgroup packs into its own columns) and feed the dV and
@@ -30,12 +32,14 @@ namespace {
 
 template <int D>
 struct BwdCfg {
-  static constexpr int kTile = 128 * D * 2;
+  static constexpr int kTile = 128 * D * 2;   // one 128-row bf16 tile
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kStage0 = 2 * kTile;          // two stages of {Q, dO}
-  static constexpr int kDS = kStage0 + 4 * kTile;    // dS^T, 128 x 128 bf16
-  static constexpr int kStat = kDS + 32768;          // per stage: lse2[128], delta[128] (TMA)
+  static constexpr int kQ0 = 2 * kTile;       // two Q stages
+  static constexpr int kDO = 4 * kTile;       // one dO buffer
+  static constexpr int kDS = 5 * kTile;       // dS^T, 128 x 128 bf16
+  static constexpr int kStg = kDS + 32768;    // dQ staging, 128 rows x 64 fp32
+  static constexpr int kStat = kStg + 32768;  // per Q stage: lse2[128], delta[128]
   static constexpr int kBar = kStat + 2 * 1024;
   static constexpr int kSmem = kBar + 256;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
@@ -70,7 +74,7 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 template <int D>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     ring_bwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
@@ -83,19 +87,22 @@ __global__ void __launch_bounds__(384, 1)
     return;
   }
   const uint32_t s0 = smem_u32(smem);
-  const uint32_t sK = s0 + C::kK, sV = s0 + C::kV, sSt = s0 + C::kStage0, sDS = s0 + C::kDS;
+  const uint32_t sK = s0 + C::kK, sV = s0 + C::kV, sQ = s0 + C::kQ0, sDO = s0 + C::kDO, sDS = s0 + C::kDS;
+  const uint32_t sStg = s0 + C::kStg;
   float* stat = reinterpret_cast<float*>(smem + C::kStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   const uint32_t b_kv = smem_u32(bars + 0);
-  const uint32_t b_full = smem_u32(bars + 1);    // [2]
-  const uint32_t b_empty = smem_u32(bars + 3);   // [2]
-  const uint32_t b_s = smem_u32(bars + 5);
-  const uint32_t b_dp = smem_u32(bars + 6);
-  const uint32_t b_pr = smem_u32(bars + 7);      // P^T, dS^T written (128 arrivals)
-  const uint32_t b_dq = smem_u32(bars + 8);      // dQ_i in TMEM (and all earlier MMAs done)
-  const uint32_t b_dqf = smem_u32(bars + 9);     // dQ_i read out (128 arrivals)
-  const uint32_t b_drain = smem_u32(bars + 10);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  const uint32_t b_qfull = smem_u32(bars + 1);   // [2] Q_i + LSE/Delta landed
+  const uint32_t b_qempty = smem_u32(bars + 3);  // [2] Q stage released (after dK_i)
+  const uint32_t b_dofull = smem_u32(bars + 5);  // dO_i landed
+  const uint32_t b_doempty = smem_u32(bars + 6); // dO released (after dV_i)
+  const uint32_t b_s = smem_u32(bars + 7);       // S^T_i in TMEM
+  const uint32_t b_dp = smem_u32(bars + 8);      // dP^T_i in TMEM
+  const uint32_t b_pr = smem_u32(bars + 9);      // P^T, dS^T written (256 arrivals)
+  const uint32_t b_dq = smem_u32(bars + 10);     // dQ_i in TMEM (and all earlier MMAs done)
+  const uint32_t b_dqf = smem_u32(bars + 11);    // dQ_i read out (128 arrivals)
+  const uint32_t b_drain = smem_u32(bars + 12);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -111,12 +118,13 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    mbar_init(b_full, 1); mbar_init(b_full + 8, 1);
-    mbar_init(b_empty, 1); mbar_init(b_empty + 8, 1);
+    mbar_init(b_qfull, 1); mbar_init(b_qfull + 8, 1);
+    mbar_init(b_qempty, 1); mbar_init(b_qempty + 8, 1);
+    mbar_init(b_dofull, 1); mbar_init(b_doempty, 1);
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
     mbar_init(b_pr, 256);
     mbar_init(b_dq, 1);
-    mbar_init(b_dqf, 256);
+    mbar_init(b_dqf, 128);
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -130,12 +138,21 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const Abort ab{abort_flag, p.status};
+  // all lanes of a warp take the same branch after a bounded wait
+  auto wait_warp = [&](uint32_t bar, uint32_t parity, int site) -> bool {
+    return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, site)) != 0;
+  };
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  // Register split: 512 threads x 128 at launch = 65536.  Producer/MMA
+  // warpgroup 80, compute warpgroups 168, dQ warpgroup 88:
+  // 128 x 80 + 256 x 168 + 128 x 88 = 64512.  Each warpgroup sets its limit at
+  // the head of its own branch.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 80;");
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       bool ok = true;
-      int issued = 0;
+      int issued_q = 0, issued_do = 0;
       tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmL); tma_prefetch_desc(&tmD);
       mbar_expect_tx(b_kv, 2 * C::kTile);
@@ -145,35 +162,34 @@ __global__ void __launch_bounds__(384, 1)
       }
       for (int i = 0; i < npairs; ++i) {
         const int st = i & 1;
-        const uint32_t ph = (i >> 1) & 1;
-        if (!mbar_wait(b_empty + 8 * st, ph ^ 1, ab, 201)) { ok = false; break; }
         const int h = pl.head(i), q0 = pl.start(i);
-        const uint32_t sq = sSt + st * 2 * C::kTile, sdo = sq + C::kTile;
+        if (!mbar_wait(b_qempty + 8 * st, ((i >> 1) & 1) ^ 1, ab, 201)) { ok = false; break; }
+        const uint32_t sq = sQ + st * C::kTile;
         const uint32_t sl = smem_u32(stat + st * 256);
-        mbar_expect_tx(b_full + 8 * st, 2 * C::kTile + 2 * 512);
-        for (int hf = 0; hf < D / 64; ++hf) {
-          tma_load_3d(sq + hf * 16384, &tmQ, b_full + 8 * st, 64 * hf, h, q0);
-          tma_load_3d(sdo + hf * 16384, &tmDO, b_full + 8 * st, 64 * hf, h, q0);
-        }
+        mbar_expect_tx(b_qfull + 8 * st, C::kTile + 2 * 512);
+        for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(sq + hf * 16384, &tmQ, b_qfull + 8 * st, 64 * hf, h, q0);
         // LSE (log2 units) and Delta of the tile's 128 query columns
-        tma_load_2d(sl, &tmL, b_full + 8 * st, q0, h);
-        tma_load_2d(sl + 512, &tmD, b_full + 8 * st, q0, h);
-        ++issued;
+        tma_load_2d(sl, &tmL, b_qfull + 8 * st, q0, h);
+        tma_load_2d(sl + 512, &tmD, b_qfull + 8 * st, q0, h);
+        ++issued_q;
+        if (!mbar_wait(b_doempty, (i & 1) ^ 1, ab, 206)) { ok = false; break; }
+        mbar_expect_tx(b_dofull, C::kTile);
+        for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(sDO + hf * 16384, &tmDO, b_dofull, 64 * hf, h, q0);
+        ++issued_do;
       }
-      if (!ok) {
+      if (!ok) {  // drain this CTA's copies still in flight
         mbar_wait_drain(b_kv, 0);
-        for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
-          mbar_wait_drain(b_full + 8 * (i & 1), (i >> 1) & 1);
+        for (int i = issued_q > 2 ? issued_q - 2 : 0; i < issued_q; ++i)
+          mbar_wait_drain(b_qfull + 8 * (i & 1), (i >> 1) & 1);
+        if (issued_do > 0) mbar_wait_drain(b_dofull, (issued_do - 1) & 1);
       }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    // Per pair i:  [dQ_{i-1} read out] dP_i | [P_i, dS_i written] dV_i, S_{i+1}, dK_i, dQ_i.
-    // S_{i+1} goes right after dV_i (the last reader of P_i in the S region), so
-    // the next pair's P phase overlaps dK_i and dQ_i.
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
+      // Per pair i: [dQ_{i-1} read out] dP_i | [P_i, dS_i written] dV_i,
+      // S_{i+1}, dK_i, dQ_i.  S_{i+1} goes right after dV_i (the last reader of
+      // P_i in the S region), so the next pair's P phase overlaps dK_i and dQ_i.
       auto issue_s = [&](int i) {  // S^T_i = K Q_i^T
-        const uint32_t sq = sSt + (i & 1) * 2 * C::kTile;
+        const uint32_t sq = sQ + (i & 1) * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -184,7 +200,7 @@ __global__ void __launch_bounds__(384, 1)
       };
       bool ok = mbar_wait(b_kv, 0, ab, 202);
       if (ok && npairs > 0) {
-        ok = mbar_wait(b_full, 0, ab, 203);
+        ok = mbar_wait(b_qfull, 0, ab, 203);
         if (ok) {
           tc_fence_after();
           issue_s(0);
@@ -193,16 +209,17 @@ __global__ void __launch_bounds__(384, 1)
       for (int i = 0; i < npairs && ok; ++i) {
         const int st = i & 1;
         const uint32_t pi = i & 1;
-        const uint32_t sq = sSt + st * 2 * C::kTile, sdo = sq + C::kTile;
+        const uint32_t sq = sQ + st * C::kTile;
         // dP^T = V dO^T, once dQ_{i-1} has left this tensor-memory region
         if (i > 0) {
           if (!mbar_wait(b_dqf, pi ^ 1, ab, 204)) { ok = false; break; }
-          tc_fence_after();
         }
+        if (!mbar_wait(b_dofull, pi, ab, 207)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::tP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sdo + off, 16, 1024), C::kIdescS,
+          umma_ss(tmem + C::tP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), C::kIdescS,
                   kk > 0);
         }
         umma_commit(b_dp);
@@ -213,9 +230,10 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                  sdesc_sw128(sdo + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                  sdesc_sw128(sDO + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(b_doempty);
         if (i + 1 < npairs) {
-          if (!mbar_wait(b_full + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
+          if (!mbar_wait(b_qfull + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
           tc_fence_after();
           issue_s(i + 1);
         }
@@ -224,7 +242,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + C::tdK, tmem + C::tP + (kk >> 2) * 64 + (kk & 3) * 8,
                   sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_empty + 8 * st);
+        umma_commit(b_qempty + 8 * st);
         // dQ_i = dS K   (A = dS from shared memory, MN-major; B = K, MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
@@ -232,16 +250,17 @@ __global__ void __launch_bounds__(384, 1)
                   C::kIdescQ, kk > 0);
         umma_commit(b_dq);
       }
-      if (!ok) {
+      if (!ok) {  // let issued MMAs finish before tensor memory is released
         umma_commit(b_drain);
         mbar_wait_drain(b_drain, 0);
       }
     }
-  } else if (warp >= 4) {
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 168;");
     // ------------------------------------------------------------ compute warpgroups
     // Two warpgroups split every 128-column tile: warpgroup w takes query
     // columns [64w, 64w + 64) of S^T/dP^T, and head-dim columns [D/2 w, D/2 (w+1))
-    // of dQ, dK and dV.  TMEM lanes: key rows for S^T/dP^T/dK/dV, query rows for dQ.
+    // of the final dK and dV.  TMEM lanes = key rows.
     const int wg = (warp - 4) >> 2;
     const int tid = threadIdx.x - 128 * (1 + wg);
     const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
@@ -250,56 +269,8 @@ __global__ void __launch_bounds__(384, 1)
     const int krow = it.k0 + tid;
     const float sl2 = p.scale_log2, scale = p.scale;
     constexpr int DH = D / 2;  // head-dim columns per warpgroup
-    bool ok = true;
-    // dQ_j, this warpgroup's head-dim half: read out of tensor memory, staged
-    // 16 columns at a time and added into the fp32 accumulator by bulk tensor
-    // reductions.  Each warp stages only its own 32 rows, in the 4 KB of the
-    // dS buffer that it also writes dS^T to, split into two 2 KB halves used
-    // alternately (64-byte swizzle): a round waits only for the reads of the
-    // round before last, and no warp waits for another.  Rows outside the
-    // query range carry exact zeros (their dS columns are masked); rows past T
-    // are clipped by the tensor map.
     const uint32_t row_addr = sDS + wg * 16384 + tid * 128;
-    const uint32_t warp_box = sDS + wg * 16384 + (tid & ~31) * 128;
-    const uint32_t half_row = (uint32_t)lane * 64;
-    const uint32_t swz64 = (uint32_t)((lane >> 1) & 3);
-    const bool lead = lane == 0;
-    // all lanes of a warp take the same branch after a bounded wait
-    auto wait_warp = [&](uint32_t bar, uint32_t parity, int site) -> bool {
-      return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, site)) != 0;
-    };
-    auto dq_out = [&](int j) -> bool {
-      if (!wait_warp(b_dq, j & 1, 220)) return false;
-      tc_fence_after();
-      uint32_t r[DH / 32][32];
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) tmem_ld32(tP + wg * DH + 32 * c, r[c]);
-      tmem_ld_wait();
-#pragma unroll
-      for (int c = 0; c < DH / 32; ++c) reg_fence32(r[c]);
-      tc_fence_before();
-      mbar_arrive(b_dqf);
-#pragma unroll
-      for (int c = 0; c < DH / 16; ++c) {
-        const uint32_t buf = warp_box + (c & 1) * 2048;
-        if (lead) bulk_wait_read_all_but_one();  // this half's previous box has been read
-        __syncwarp();
-#pragma unroll
-        for (int pc = 0; pc < 4; ++pc) {
-          const int x = 16 * (c & 1) + 4 * pc;
-          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(buf + half_row + ((pc ^ swz64) << 4)),
-                       "r"(r[c >> 1][x]), "r"(r[c >> 1][x + 1]), "r"(r[c >> 1][x + 2]), "r"(r[c >> 1][x + 3])
-                       : "memory");
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lead) {
-          tma_reduce_add_3d(&tmDQ, buf, wg * DH + 16 * c, pl.head(j), pl.start(j) + (tid & ~31));
-          bulk_commit();
-        }
-      }
-      return true;
-    };
+    bool ok = true;
     for (int i = 0; i < npairs && ok; ++i) {
       const int st = i & 1;
       const uint32_t pi = i & 1;
@@ -345,8 +316,6 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st16(tS + 64 * wg, w0);
         tmem_st16(tS + 64 * wg + 16, w1);
       }
-      // ---- dQ of the previous pair (frees the dP region for dP^T_i)
-      if (i > 0 && !dq_out(i - 1)) { ok = false; break; }
       // ---- dS^T = scale P^T (dP^T - Delta)
       if (!wait_warp(b_dp, pi, 211)) { ok = false; break; }
       tc_fence_after();
@@ -357,7 +326,6 @@ __global__ void __launch_bounds__(384, 1)
         tmem_ld_wait();
         reg_fence32(r[0]);
         reg_fence32(r[1]);
-        // this warpgroup's 64 query columns are chunk `wg` of the MN-major dS tile
         uint32_t w[2][16];
 #pragma unroll
         for (int c = 0; c < 2; ++c) {
@@ -373,9 +341,9 @@ __global__ void __launch_bounds__(384, 1)
           }
           tmem_st16(tP + 64 * wg + 16 * c, w[c]);
         }
-        // the TMA must have read this warp's staged dQ rows before they are rewritten
-        if (lead) bulk_wait_read();
-        __syncwarp();
+        // dS^T to shared memory (this warpgroup's 64 query columns are chunk `wg`
+        // of the MN-major dS tile), once the dQ MMA of the previous pair has read it
+        if (i > 0 && !wait_warp(b_dq, pi ^ 1, 212)) { ok = false; break; }
 #pragma unroll
         for (int c = 0; c < 2; ++c)
 #pragma unroll
@@ -391,9 +359,9 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_before();
       mbar_arrive(b_pr);
     }
-    if (ok && npairs > 0) ok = dq_out(npairs - 1);  // also: every MMA of the CTA is done
-    if (lead) bulk_wait_all();
-    if (ok && npairs > 0) {
+    // every MMA of the CTA is done once the last dQ has landed
+    if (ok && npairs > 0 && wait_warp(b_dq, (npairs - 1) & 1, 213)) {
+      tc_fence_after();
       const bool valid = krow < it.k1;
       float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
       float* dk_row = p.dk_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
@@ -416,6 +384,56 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     }
+  } else {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
+    // ------------------------------------------------------------ dQ warpgroup
+    // TMEM lanes = query rows.  For every pair: read dQ_i (64 columns at a
+    // time), stage it in this warpgroup's buffer (each warp its own 32 rows,
+    // two 32-column boxes per 64 columns, 128-byte swizzle) and add it into the
+    // fp32 accumulator with bulk tensor reductions.  Rows outside the query
+    // range carry exact zeros (their dS columns are masked); rows past T are
+    // clipped by the tensor map.
+    const int tid = threadIdx.x - 384;
+    const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
+    const uint32_t tQ = tmem_addr(tmem, lane_base, C::tP);
+    const uint32_t wbuf = sStg + (uint32_t)(warp & 3) * 8192;  // this warp's 8 KB
+    const uint32_t row = (uint32_t)lane * 128;
+    const bool lead = lane == 0;
+    for (int j = 0; j < npairs; ++j) {
+      if (!wait_warp(b_dq, j & 1, 220)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int half = 0; half < D / 64; ++half) {
+        uint32_t r[2][32];
+        tmem_ld32(tQ + 64 * half, r[0]);
+        tmem_ld32(tQ + 64 * half + 32, r[1]);
+        tmem_ld_wait();
+        reg_fence32(r[0]);
+        reg_fence32(r[1]);
+        if (half == D / 64 - 1) {  // all of dQ_j is in registers or staged: release tensor memory
+          tc_fence_before();
+          mbar_arrive(b_dqf);
+        }
+        if (lead) bulk_wait_read();  // the buffer's previous boxes have been read
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+#pragma unroll
+          for (int pc = 0; pc < 8; ++pc)
+            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(wbuf + k * 4096 + row +
+                                                                          ((pc ^ (lane & 7)) << 4)),
+                         "r"(r[k][4 * pc]), "r"(r[k][4 * pc + 1]), "r"(r[k][4 * pc + 2]), "r"(r[k][4 * pc + 3])
+                         : "memory");
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lead) {
+          tma_reduce_add_3d(&tmDQ, wbuf, 64 * half, pl.head(j), pl.start(j) + (tid & ~31));
+          tma_reduce_add_3d(&tmDQ, wbuf + 4096, 64 * half + 32, pl.head(j), pl.start(j) + (tid & ~31));
+          bulk_commit();
+        }
+      }
+    }
+    if (lead) bulk_wait_all();
   }
 
   __syncwarp();
@@ -436,7 +454,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, 384, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, p);
+  kern<<<(unsigned)grid, 512, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, p);
   return cudaGetLastError();
 }
 
