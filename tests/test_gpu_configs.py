@@ -1,0 +1,131 @@
+"""GPU parity on the full-size workloads, in the launch configuration bench.py times.
+
+The oracle cannot run these sizes in full, so outputs are checked on sampled
+query rows (exact per-row O, LSE and dq from the oracle, O(L d) per row) and
+through identities that hold at any size:
+  sum_j dv_j = sum over the group's query heads of sum_i dO_i,  sum_j dk_j = 0
+(per document).  Tolerances: 2e-2 on O/dq with fp32 outputs, 1e-3 on LSE, and
+ring vs cp_size = 1 on the GPU within 1e-3 (fp32 outputs; the backward is
+compared on one shared saved (O, LSE), see test_gpu_bwd).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as A
+from workloads import draw_qkvdo, workload
+
+pytestmark = pytest.mark.gpu
+
+O_TOL, LSE_TOL, RING_TOL = 2e-2, 1e-3, 1e-3
+
+_cache = {}
+
+
+@pytest.fixture(scope="module")
+def ra():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import context_ring_attention_step_gb300 as m
+    m.load_library()
+    return m
+
+
+def _inputs(wl):
+    key = (wl.T, wl.Hq, wl.Hkv, wl.d, wl.seed)
+    if key not in _cache:
+        _cache.clear()
+        _cache[key] = draw_qkvdo(wl)
+    return _cache[key]
+
+
+def _run(ra, wl, cps=None, layout=None):
+    q, k, v, do = _inputs(wl)
+    cps = list(wl.cp_per_doc) if cps is None else cps
+    layout = layout or wl.layout
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    plan = ra.Plan(wl.cu_seqlens, cps, layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    o, lse = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, layout, wl.causal, wl.softmax_scale,
+                              o_fp32=True, plan=plan, check=True)
+    dq, dk, dv = ra.ring_attn_bwd(qd, kd, vd, o, dod, lse, wl.cu_seqlens, cps, layout, wl.causal,
+                                  wl.softmax_scale, grads_fp32=True, plan=plan, check=True)
+    torch.cuda.synchronize()
+    return o, lse, dq, dk, dv
+
+
+def _sample_rows(wl, rng, n):
+    cu = wl.cu_seqlens
+    rows = set(rng.integers(0, wl.T, n).tolist())
+    for d in range(wl.num_docs):  # document edges and shard edges of the first doc
+        if cu[d + 1] > cu[d]:
+            rows.update({cu[d], cu[d + 1] - 1})
+    return sorted(rows)
+
+
+def _check(ra, wl, heads, nrows, cps=None, layout=None):
+    q, k, v, do = _inputs(wl)
+    o, lse, dq, dk, dv = _run(ra, wl, cps, layout)
+    o, lse, dq = o.cpu().numpy(), lse.cpu().numpy(), dq.cpu().numpy()
+    rng = np.random.default_rng(wl.seed)
+    G = wl.Hq // wl.Hkv
+    for h in heads:
+        rows = _sample_rows(wl, rng, nrows)
+        # one query head and its kv head, so the oracle converts only what it reads
+        qh, dh = q[:, h:h + 1].contiguous(), do[:, h:h + 1].contiguous()
+        kh, vh = k[:, h // G:h // G + 1].contiguous(), v[:, h // G:h // G + 1].contiguous()
+        ro, rl = A.attention_rows(qh, kh, vh, wl.cu_seqlens, rows, 0, wl.causal, wl.softmax_scale)
+        rdq = A.attention_rows_dq(qh, kh, vh, dh, wl.cu_seqlens, rows, 0, wl.causal, wl.softmax_scale)
+        assert np.abs(o[rows, h] - ro).max() <= O_TOL, (wl.name, h)
+        assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL, (wl.name, h)
+        assert np.abs(dq[rows, h] - rdq).max() <= O_TOL, (wl.name, h)
+    dk, dv = dk.double(), dv.double()
+    dof = do.cuda().double()
+    cu = wl.cu_seqlens
+    for d in range(wl.num_docs):
+        b, e = cu[d], cu[d + 1]
+        if e == b:
+            continue
+        for g in range(wl.Hkv):
+            want = dof[b:e, g * G:(g + 1) * G].sum(dim=(0, 1))
+            # the identities hold for exact P and dS; the bf16 rounding of P and
+            # dS (about 2^-9 relative, unbiased) leaves a residue that grows with
+            # the square root of the (e - b) G rows summed
+            tol = 1e-2 * np.sqrt((e - b) * G) + 1e-2
+            assert (dv[b:e, g].sum(dim=0) - want).abs().max().item() <= tol, (wl.name, d, g)
+            assert dk[b:e, g].sum(dim=0).abs().max().item() <= tol, (wl.name, d, g)
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+def test_long_128k(ra, layout):
+    wl = workload("long_128k_" + layout)
+    _check(ra, wl, heads=(0, 17, 31), nrows=24)
+
+
+def test_varlen_65k(ra):
+    _check(ra, workload("varlen_65k"), heads=(0, 9, 30), nrows=48)
+
+
+def test_max_256k(ra):
+    _check(ra, workload("max_256k"), heads=(0, 31), nrows=16)
+
+
+def test_ring_equals_cp1_at_128k(ra):
+    """Full-tensor comparison of the 16-step zigzag ring with cp_size = 1 (fp32 outputs)."""
+    wl = workload("long_128k")
+    q, k, v, do = (x.cuda() for x in _inputs(wl))
+    plan1 = ra.Plan(wl.cu_seqlens, [1], "zigzag", True, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan16 = ra.Plan(wl.cu_seqlens, [16], "zigzag", True, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    o1, l1 = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, [1], "zigzag", True, wl.softmax_scale, o_fp32=True,
+                              plan=plan1, check=True)
+    o16, l16 = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, [16], "zigzag", True, wl.softmax_scale, o_fp32=True,
+                                plan=plan16, check=True)
+    assert (o16 - o1).abs().max().item() <= RING_TOL
+    assert (l16 - l1).abs().max().item() <= RING_TOL
+    del o16, l16
+    g1 = ra.ring_attn_bwd(q, k, v, o1, do, l1, wl.cu_seqlens, [1], "zigzag", True, wl.softmax_scale,
+                          grads_fp32=True, plan=plan1, check=True)
+    g16 = ra.ring_attn_bwd(q, k, v, o1, do, l1, wl.cu_seqlens, [16], "zigzag", True, wl.softmax_scale,
+                           grads_fp32=True, plan=plan16, check=True)
+    for name, a, b in zip(("dq", "dk", "dv"), g16, g1):
+        assert (a - b).abs().max().item() <= RING_TOL, name
