@@ -53,6 +53,42 @@ def peaks():
         return 1900.0, 1700.0, 6800.0, "fallback"
 
 
+KERNEL_SOURCES = {
+    "ring_fwd_step_kernel": ("fwd.cu", "tc.cuh", "ring_attn_internal.h"),
+    "ring_bwd_step_kernel": ("bwd.cu", "tc.cuh", "ring_attn_internal.h"),
+}
+
+
+def kernel_source_hash(kernel):
+    """sha256 (first 16 hex digits) of the sources a kernel is built from."""
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "context_ring_attention_step_gb300", "csrc")
+    for f in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel, workload_name):
+    """DRAM bytes per launch of `kernel` from the committed ncu summary of this
+    workload, or None when there is none or the kernel changed since."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic_%s.md" % workload_name)
+    try:
+        lines = open(path).read().splitlines()
+    except OSError:
+        return None
+    want = kernel_source_hash(kernel)
+    for line in lines:
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) >= 4 and cells[0] == kernel:
+            try:
+                return float(cells[2]) if cells[3] == want else None
+            except ValueError:
+                return None
+    return None
+
+
 def max_over_ranks(ms, dist=None, device=None):
     """Max of a per-rank time over all ranks (identity on one process)."""
     if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
@@ -358,7 +394,8 @@ def main():
     achieved = alg_flops_per_launch / avg_launch_s / 1e12
     roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak_s, "unit": "TFLOP/s",
             "frac": achieved / peak_s, "peak_kind": peak_kind + " bf16 sustained (kernel timed inside a long step)",
-            "frac_of_burst_peak": achieved / peak_b, "traffic": None,
+            "frac_of_burst_peak": achieved / peak_b, "traffic": recorded_traffic(name, wl.name),
+            "traffic_unit": "bytes per launch (dram read + write, ncu)",
             "per_launch_flops": alg_flops_per_launch, "avg_launch_ms": avg_launch_s * 1e3}
 
     # ---------------------------------------------------------------- end to end (host buffers)

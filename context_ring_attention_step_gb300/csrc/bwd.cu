@@ -18,7 +18,8 @@
 //                (P^T, dS^T) and, at the end, half of the head dimension of dK/dV
 //   warps 12-15  dQ warpgroup: reads dQ_i out of tensor memory, stages it in its
 //                own shared-memory buffer and adds it into the accumulator with
-//                bulk reductions, off the compute warpgroups' path
+//                bulk reductions, off the compute warpgroups' path; every kChain
+//                pairs it also moves the dV/dK chain into the fp32 accumulators
 // Tensor memory: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T/dQ after.
 // P^T and dS^T (bf16, two per column) overwrite columns [0,32) and [64,96) of
 // S^T and dP^T (each warpgroup packs into its own columns) and feed the dV and
@@ -46,6 +47,12 @@ struct BwdCfg {
   static constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);   // dV, dK: A tmem, B MN-major
   static constexpr uint32_t kIdescQ = idesc_bf16_f32(128, D, true, true);    // dQ: A, B MN-major
   static constexpr uint32_t tdV = 0, tdK = D, tS = 2 * D, tP = 2 * D + 128;
+  // dV/dK are accumulated in tensor memory over at most kChain pairs, then
+  // added into the fp32 accumulators.  The tensor core's fp32 accumulation
+  // drifts roughly in proportion to the chain length (4096 pairs: 6.6e-4
+  // relative on the first keys of a 128K document); 256 pairs bound it near
+  // 4e-5 and cover every CTA of a 16-step 128K ring without a flush.
+  static constexpr int kChain = 256;
 };
 
 // Query tiles of the CTA's pairs.  Tiles of a range start at the range start
@@ -102,7 +109,8 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t b_dq = smem_u32(bars + 10);     // dQ_i in TMEM (and all earlier MMAs done)
   const uint32_t b_dqf = smem_u32(bars + 11);    // dQ_i read out (128 arrivals)
   const uint32_t b_drain = smem_u32(bars + 12);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  const uint32_t b_kvf = smem_u32(bars + 13);    // a finished dV/dK chain left tensor memory (128 arrivals)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -126,6 +134,7 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(b_dq, 1);
     mbar_init(b_dqf, 128);
     mbar_init(b_drain, 1);
+    mbar_init(b_kvf, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -224,13 +233,16 @@ __global__ void __launch_bounds__(512, 1)
         }
         umma_commit(b_dp);
         if (!mbar_wait(b_pr, pi, ab, 205)) { ok = false; break; }
+        if (i > 0 && i % C::kChain == 0) {  // the previous dV/dK chain has been flushed
+          if (!mbar_wait(b_kvf, ((i / C::kChain) - 1) & 1, ab, 208)) { ok = false; break; }
+        }
         tc_fence_after();
         // dV += P^T dO   (A from tensor memory: packed query columns 0-63 in
         // columns [0,32) of the S region, 64-127 in columns [64,96); B MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                  sdesc_sw128(sDO + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                  sdesc_sw128(sDO + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_doempty);
         if (i + 1 < npairs) {
           if (!mbar_wait(b_qfull + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
@@ -241,7 +253,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + C::tdK, tmem + C::tP + (kk >> 2) * 64 + (kk & 3) * 8,
-                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i > 0 || kk > 0) ? 1u : 0u);
+                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_qempty + 8 * st);
         // dQ_i = dS K   (A = dS from shared memory, MN-major; B = K, MN-major)
 #pragma unroll
@@ -270,6 +282,31 @@ __global__ void __launch_bounds__(512, 1)
     const float sl2 = p.scale_log2, scale = p.scale;
     constexpr int DH = D / 2;  // head-dim columns per warpgroup
     const uint32_t row_addr = sDS + wg * 16384 + tid * 128;
+    // add this warpgroup's half of dV and dK (tensor memory, lanes = key rows)
+    // into the fp32 accumulators
+    const bool valid = krow < it.k1;
+    float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
+    float* dk_row = p.dk_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
+    auto flush_dkdv = [&]() {
+#pragma unroll
+      for (int which = 0; which < 2; ++which) {
+        const uint32_t t = tmem_addr(tmem, lane_base, (which == 0 ? C::tdV : C::tdK) + wg * DH);
+        float* dst = which == 0 ? dv_row : dk_row;
+#pragma unroll
+        for (int c = 0; c < DH / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(t + 32 * c, r);
+          tmem_ld_wait();
+          reg_fence32(r);
+          if (valid) {
+#pragma unroll
+            for (int x = 0; x < 8; ++x)
+              red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                         __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+          }
+        }
+      }
+    };
     bool ok = true;
     for (int i = 0; i < npairs && ok; ++i) {
       const int st = i & 1;
@@ -362,27 +399,7 @@ __global__ void __launch_bounds__(512, 1)
     // every MMA of the CTA is done once the last dQ has landed
     if (ok && npairs > 0 && wait_warp(b_dq, (npairs - 1) & 1, 213)) {
       tc_fence_after();
-      const bool valid = krow < it.k1;
-      float* dv_row = p.dv_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
-      float* dk_row = p.dk_acc + ((size_t)krow * p.Hkv + g) * D + wg * DH;
-#pragma unroll
-      for (int which = 0; which < 2; ++which) {
-        const uint32_t t = tmem_addr(tmem, lane_base, (which == 0 ? C::tdV : C::tdK) + wg * DH);
-        float* dst = which == 0 ? dv_row : dk_row;
-#pragma unroll
-        for (int c = 0; c < DH / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(t + 32 * c, r);
-          tmem_ld_wait();
-          reg_fence32(r);
-          if (valid) {
-#pragma unroll
-            for (int x = 0; x < 8; ++x)
-              red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
-                         __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
-          }
-        }
-      }
+      flush_dkdv();
     }
   } else {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
@@ -431,6 +448,33 @@ __global__ void __launch_bounds__(512, 1)
           tma_reduce_add_3d(&tmDQ, wbuf + 4096, 64 * half + 32, pl.head(j), pl.start(j) + (tid & ~31));
           bulk_commit();
         }
+      }
+      // pair j closed a dV/dK chain (all of its MMAs are done: b_dq of pair j)
+      // and more pairs follow: add the chain into the fp32 accumulators, so the
+      // MMA can restart the chain in tensor memory.  Here lanes = key rows.
+      if ((j + 1) % C::kChain == 0 && j + 1 < npairs) {
+        const int krow = it.k0 + tid;
+        const bool valid = krow < it.k1;
+#pragma unroll
+        for (int which = 0; which < 2; ++which) {
+          const uint32_t t = tmem_addr(tmem, lane_base, which == 0 ? C::tdV : C::tdK);
+          float* dst = (which == 0 ? p.dv_acc : p.dk_acc) + ((size_t)krow * p.Hkv + g) * D;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(t + 32 * c, r);
+            tmem_ld_wait();
+            reg_fence32(r);
+            if (valid) {
+#pragma unroll
+              for (int x = 0; x < 8; ++x)
+                red_add_v4(dst + 32 * c + 4 * x, __uint_as_float(r[4 * x]), __uint_as_float(r[4 * x + 1]),
+                           __uint_as_float(r[4 * x + 2]), __uint_as_float(r[4 * x + 3]));
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(b_kvf);
       }
     }
     if (lead) bulk_wait_all();
