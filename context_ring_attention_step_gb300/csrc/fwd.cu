@@ -62,9 +62,10 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t b_full = smem_u32(bars + 1);                      // [kStages]
   const uint32_t b_empty = smem_u32(bars + 1 + C::kStages);        // [kStages]
   const uint32_t b_s = smem_u32(bars + 1 + 2 * C::kStages);        // [2] S ready / O final
-  const uint32_t b_p = smem_u32(bars + 3 + 2 * C::kStages);        // [2] P written
-  const uint32_t b_drain = smem_u32(bars + 5 + 2 * C::kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6 + 2 * C::kStages);
+  const uint32_t b_p = smem_u32(bars + 3 + 2 * C::kStages);        // [2] P keys 0-63 written
+  const uint32_t b_p2 = smem_u32(bars + 5 + 2 * C::kStages);       // [2] P keys 64-127 written
+  const uint32_t b_drain = smem_u32(bars + 7 + 2 * C::kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * C::kStages);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   // A CTA of this grid already gave up: do no work (fail fast, no waits).
@@ -102,6 +103,7 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_init(b_s, 1); mbar_init(b_s + 8, 1);
     mbar_init(b_p, 128); mbar_init(b_p + 8, 128);
+    mbar_init(b_p2, 128); mbar_init(b_p2 + 8, 128);
     mbar_init(b_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -187,14 +189,19 @@ __global__ void __launch_bounds__(384, 1)
         bool k_ready = false;
         auto pv_then_qk = [&](int qt, int na, uint32_t& pph) {
           if (!ok || j >= na) return;
-          if (!mbar_wait(b_p + 8 * qt, pph, ab, 105)) { ok = false; return; }
-          pph ^= 1;
-          tc_fence_after();
+          // P.V in two halves of 64 keys: the first half runs while the softmax
+          // still computes the second
           const uint32_t va = sKV + vst * C::kTile;
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + 256 + qt * D, tmem + qt * 128 + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024),
-                    C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int hf = 0; hf < 2; ++hf) {
+            if (!mbar_wait((hf ? b_p2 : b_p) + 8 * qt, pph, ab, 105 + 3 * hf)) { ok = false; return; }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
+              umma_ts(tmem + 256 + qt * D, tmem + qt * 128 + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024),
+                      C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          pph ^= 1;
           if (j + 1 < na) {
             if (!k_ready) {
               if (!mbar_wait(b_full + 8 * stage, kph, ab, 106)) { ok = false; return; }
@@ -234,6 +241,7 @@ __global__ void __launch_bounds__(384, 1)
     const int row0 = it.q0 + 128 * qt;
     const int row = row0 + tid;
     const float sl2 = p.scale_log2;
+    const uint64_t sl2x2 = f2_pack(sl2, sl2);
     float m_ref = kNegInf, l_sum = 0.f, l_rnd = 0.f;
     uint32_t sph = 0;
     bool ok = true;
@@ -283,27 +291,36 @@ __global__ void __launch_bounds__(384, 1)
       const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
       // Two row sums: of P (for the LSE) and of the bf16-rounded P that the PV MMA
       // consumes (to normalise O, so O stays an exact convex combination of V).
-      float ls0 = 0.f, ls1 = 0.f, lr0 = 0.f, lr1 = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      // Scale-and-shift and the exact sum run on packed fp32 pairs; the rounded
+      // sum adds the bf16 halves straight into fp32.
+      const uint64_t nm2 = f2_pack(-m_use, -m_use);
+      uint64_t ls_a = 0, ls_b = 0;
+      float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
+      auto p_chunk = [&](int c) {
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i]), sl2, -m_use));
-          const float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * i + 1]), sl2, -m_use));
-          ls0 += p0;
-          ls1 += p1;
+          const uint64_t x =
+              f2_fma(f2_pack(__uint_as_float(r[c][2 * i]), __uint_as_float(r[c][2 * i + 1])), sl2x2, nm2);
+          float x0, x1;
+          f2_unpack(x, x0, x1);
+          const float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           pk[i] = pack_bf16x2(p0, p1);
-          lr0 += __uint_as_float(pk[i] << 16);
-          lr1 += __uint_as_float(pk[i] & 0xffff0000u);
+          if (i & 1) {
+            ls_b = f2_add(ls_b, f2_pack(p0, p1));
+            add_bf16x2_to(lr2, lr3, pk[i]);
+          } else {
+            ls_a = f2_add(ls_a, f2_pack(p0, p1));
+            add_bf16x2_to(lr0, lr1, pk[i]);
+          }
         }
         tmem_st16(tS + 16 * c, pk);
-      }
-      l_sum += ls0 + ls1;
-      l_rnd += lr0 + lr1;
+      };
+      p_chunk(0);
+      p_chunk(1);
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1));
-        // P is already stored, so the S registers are free here.
+        // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1)),
+        // and must be rescaled before PV(j) adds to it.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -314,11 +331,20 @@ __global__ void __launch_bounds__(384, 1)
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
           tmem_st32(tO + 32 * c, o);
         }
-        tmem_st_wait();
       }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(b_p + 8 * qt);
+      p_chunk(2);
+      p_chunk(3);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(b_p2 + 8 * qt);
+      float a0, a1, b0, b1;
+      f2_unpack(ls_a, a0, a1);
+      f2_unpack(ls_b, b0, b1);
+      l_sum += (a0 + a1) + (b0 + b1);
+      l_rnd += (lr0 + lr1) + (lr2 + lr3);
     }
     if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
       if (na > 0) {
