@@ -130,11 +130,12 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(b_qempty, 1); mbar_init(b_qempty + 8, 1);
     mbar_init(b_dofull, 1); mbar_init(b_doempty, 1);
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
-    mbar_init(b_pr, 256);
+    mbar_init(b_pr, 8);    // arrivals are one per warp (8 compute warps): the shared-memory
+                           // unit takes an mbarrier's arrivals one at a time
     mbar_init(b_dq, 1);
-    mbar_init(b_dqf, 128);
+    mbar_init(b_dqf, 4);
     mbar_init(b_drain, 1);
-    mbar_init(b_kvf, 128);
+    mbar_init(b_kvf, 4);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -394,7 +395,8 @@ __global__ void __launch_bounds__(512, 1)
       tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(b_pr);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_pr);
     }
     // every MMA of the CTA is done once the last dQ has landed
     if (ok && npairs > 0 && wait_warp(b_dq, (npairs - 1) & 1, 213)) {
@@ -429,7 +431,8 @@ __global__ void __launch_bounds__(512, 1)
         reg_fence32(r[1]);
         if (half == D / 64 - 1) {  // all of dQ_j is in registers or staged: release tensor memory
           tc_fence_before();
-          mbar_arrive(b_dqf);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(b_dqf);
         }
         if (lead) bulk_wait_read();  // the buffer's previous boxes have been read
         __syncwarp();
@@ -474,7 +477,8 @@ __global__ void __launch_bounds__(512, 1)
           }
         }
         tc_fence_before();
-        mbar_arrive(b_kvf);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(b_kvf);
       }
     }
     if (lead) bulk_wait_all();

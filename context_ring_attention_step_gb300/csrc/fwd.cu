@@ -10,13 +10,15 @@
 //
 // Warp roles (384 threads):
 //   warp 0      TMA producer: Q0/Q1 once, then K_j, V_j into a ring of stages
-//   warp 1      TMEM owner + single-thread UMMA issuer
+//   warp 1      TMEM owner + UMMA issuer for Q0
+//   warp 2      UMMA issuer for Q1
 //   warps 4-7   softmax / correction / epilogue of Q0 (TMEM lanes 0-127)
 //   warps 8-11  softmax / correction / epilogue of Q1
 // Tensor memory (512 columns): S0 [0,128), S1 [128,256), O0 and O1 after that.
 // P (bf16) overwrites the first 64 columns of S and feeds the P.V MMA straight
-// from tensor memory.  MMA order per key tile j: PV0(j), S0(j+1), PV1(j),
-// S1(j+1), so one Q tile's softmax overlaps the other tile's MMAs.
+// from tensor memory.  Each Q tile's issuer runs PV(j) then S(j+1); the two
+// softmax warpgroups take turns, so one tile's softmax overlaps the other
+// tile's MMAs.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
 
@@ -25,7 +27,11 @@ namespace {
 
 #define kNegInf (-__int_as_float(0x7f800000))
 constexpr float kLn2 = 0.69314718055994530942f;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: P values stay below 2^8
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: after a max update P stays below 2^8
+// A tile computed against the running reference is kept while its row sum of
+// P stays at or below this bound (so every P <= 2^16; fp32 accumulators and
+// bf16 P have room to spare).
+constexpr float kSpecSumLimit = 65536.0f;
 
 template <int D>
 struct FwdCfg {
@@ -62,10 +68,9 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t b_full = smem_u32(bars + 1);                      // [kStages]
   const uint32_t b_empty = smem_u32(bars + 1 + C::kStages);        // [kStages]
   const uint32_t b_s = smem_u32(bars + 1 + 2 * C::kStages);        // [2] S ready / O final
-  const uint32_t b_p = smem_u32(bars + 3 + 2 * C::kStages);        // [2] P keys 0-63 written
-  const uint32_t b_p2 = smem_u32(bars + 5 + 2 * C::kStages);       // [2] P keys 64-127 written
-  const uint32_t b_drain = smem_u32(bars + 7 + 2 * C::kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 8 + 2 * C::kStages);
+  const uint32_t b_p = smem_u32(bars + 3 + 2 * C::kStages);        // [2] P written
+  const uint32_t b_drain = smem_u32(bars + 5 + 2 * C::kStages);    // [2]
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * C::kStages);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   // A CTA of this grid already gave up: do no work (fail fast, no waits).
@@ -99,12 +104,11 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(b_q, 1);
     for (int s = 0; s < C::kStages; ++s) {
       mbar_init(b_full + 8 * s, 1);
-      mbar_init(b_empty + 8 * s, 1);
+      mbar_init(b_empty + 8 * s, 2);  // one commit per MMA issuer
     }
     mbar_init(b_s, 1); mbar_init(b_s + 8, 1);
-    mbar_init(b_p, 128); mbar_init(b_p + 8, 128);
-    mbar_init(b_p2, 128); mbar_init(b_p2 + 8, 128);
-    mbar_init(b_drain, 1);
+    mbar_init(b_p, 4); mbar_init(b_p + 8, 4);  // one arrival per softmax warp
+    mbar_init(b_drain, 1); mbar_init(b_drain + 8, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -154,79 +158,67 @@ __global__ void __launch_bounds__(384, 1)
           mbar_wait_drain(b_full + 8 * (i % C::kStages), (i / C::kStages) & 1);
       }
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------ MMA issuers
+    // One issuing thread per Q tile.  A thread that has issued tcgen05.mma and
+    // then waits on a barrier is held until the tensor pipe has taken its MMAs,
+    // so with a single issuer the pipe runs dry on every wait; with two, one
+    // tile's MMAs keep it busy while the other issuer waits.  Both issuers walk
+    // every K/V stage in order (waiting for it to be full, then committing its
+    // release), so each stage release gets exactly one arrival from each.
+    const int qt = warp - 1;
     if (lane == 0) {
+      const int na = qt == 0 ? n_act[0] : n_act[1];
+      const uint32_t tS = tmem + qt * 128, tO = tmem + 256 + qt * D, qa = sQ + qt * C::kTile;
       bool ok = mbar_wait(b_q, 0, ab, 102);
       tc_fence_after();
       int stage = 0;
       uint32_t kph = 0;
       auto advance = [&]() { if (++stage == C::kStages) { stage = 0; kph ^= 1; } };
-      auto qk = [&](int qt, int kst) {
-        const uint32_t qa = sQ + qt * C::kTile, ka = sKV + kst * C::kTile;
+      auto qk = [&](int kst) {
+        const uint32_t ka = sKV + kst * C::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + qt * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024),
-                  C::kIdescQK, kk > 0);
+          umma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), C::kIdescQK, kk > 0);
         }
       };
       if (ok) ok = mbar_wait(b_full + 8 * stage, kph, ab, 103);
       if (ok) {
         tc_fence_after();
-        for (int qt = 0; qt < 2; ++qt)
-          if (n_act[qt] > 0) { qk(qt, stage); umma_commit(b_s + 8 * qt); }
+        if (na > 0) { qk(stage); umma_commit(b_s + 8 * qt); }
         umma_commit(b_empty + 8 * stage);
         advance();
       }
-      uint32_t pph0 = 0, pph1 = 0;
-      const int na0 = n_act[0], na1 = n_act[1];
+      uint32_t pph = 0;
       for (int j = 0; j < tl.n && ok; ++j) {
         const int vst = stage;
         if (!mbar_wait(b_full + 8 * vst, kph, ab, 104)) { ok = false; break; }
         tc_fence_after();
         advance();  // stage now holds K_{j+1}
-        bool k_ready = false;
-        auto pv_then_qk = [&](int qt, int na, uint32_t& pph) {
-          if (!ok || j >= na) return;
-          // P.V in two halves of 64 keys: the first half runs while the softmax
-          // still computes the second
+        if (j < na) {
+          if (!mbar_wait(b_p + 8 * qt, pph, ab, 105)) { ok = false; break; }
+          pph ^= 1;
+          tc_fence_after();
           const uint32_t va = sKV + vst * C::kTile;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            if (!mbar_wait((hf ? b_p2 : b_p) + 8 * qt, pph, ab, 105 + 3 * hf)) { ok = false; return; }
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 4 * hf; kk < 4 * hf + 4; ++kk)
-              umma_ts(tmem + 256 + qt * D, tmem + qt * 128 + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024),
-                      C::kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          }
-          pph ^= 1;
-          if (j + 1 < na) {
-            if (!k_ready) {
-              if (!mbar_wait(b_full + 8 * stage, kph, ab, 106)) { ok = false; return; }
-              tc_fence_after();
-              k_ready = true;
-            }
-            qk(qt, stage);
-          }
-          umma_commit(b_s + 8 * qt);  // S(j+1) ready, or O final after the last tile
-        };
-        pv_then_qk(0, na0, pph0);
-        pv_then_qk(1, na1, pph1);
-        if (!ok) break;
-        umma_commit(b_empty + 8 * vst);
+          for (int kk = 0; kk < 8; ++kk)
+            umma_ts(tO, tS + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), C::kIdescPV,
+                    (j > 0 || kk > 0) ? 1u : 0u);
+        }
+        umma_commit(b_empty + 8 * vst);  // V_j: free once this tile's P.V has run
         if (j + 1 < tl.n) {
-          if (!k_ready) {
-            if (!mbar_wait(b_full + 8 * stage, kph, ab, 107)) { ok = false; break; }
-          }
-          umma_commit(b_empty + 8 * stage);
+          if (!mbar_wait(b_full + 8 * stage, kph, ab, 106)) { ok = false; break; }
+          tc_fence_after();
+          if (j + 1 < na) qk(stage);
+          umma_commit(b_empty + 8 * stage);  // K_{j+1}: free once this tile's QK has run
           advance();
         }
+        if (j < na) umma_commit(b_s + 8 * qt);  // S(j+1) ready, or O final after the last tile
       }
       if (!ok) {  // let issued MMAs finish before tensor memory is released
-        umma_commit(b_drain);
-        mbar_wait_drain(b_drain, 0);
+        umma_commit(b_drain + 8 * qt);
+        mbar_wait_drain(b_drain + 8 * qt, 0);
       }
     }
   }
@@ -247,6 +239,7 @@ __global__ void __launch_bounds__(384, 1)
     bool ok = true;
     const int na = qt == 0 ? n_act[0] : n_act[1];
     const bool qa = qt == 0 ? q_act[0] : q_act[1];
+    const int na_other = qt == 0 ? n_act[1] : n_act[0];
     for (int j = 0; j < na; ++j) {
       if (!mbar_wait(b_s + 8 * qt, sph, ab, 110)) { ok = false; break; }
       sph ^= 1;
@@ -256,7 +249,14 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tS + 32, r[1]);
       tmem_ld32(tS + 64, r[2]);
       tmem_ld32(tS + 96, r[3]);
+      // The two softmax warpgroups take turns (Q0 tile j after Q1 tile j-1, Q1
+      // tile j after Q0 tile j): each then runs alone on the SM's schedulers,
+      // and their MMAs reach the tensor pipe interleaved instead of together.
+      const int k_other = j - (qt == 0 ? 1 : 0);
+      const bool turn = k_other < 0 || k_other >= na_other ||
+                        mbar_wait(b_p + 8 * (1 - qt), (uint32_t)k_other & 1u, ab, 112);
       tmem_ld_wait();
+      if (!turn) { ok = false; break; }
       reg_fence32(r[0]); reg_fence32(r[1]); reg_fence32(r[2]); reg_fence32(r[3]);
       const int kst = tl.start(j), kend = tl.end(j);
       const bool need_mask = (kst + 128 > kend) || (p.causal && kst + 127 > row0);
@@ -266,35 +266,11 @@ __global__ void __launch_bounds__(384, 1)
         for (int c = 0; c < 128; ++c)
           if (kst + c > lim) r[c >> 5][c & 31] = __float_as_uint(kNegInf);
       }
-      float mx0 = kNegInf, mx1 = kNegInf, mx2 = kNegInf, mx3 = kNegInf;
-#pragma unroll
-      for (int c = 0; c < 32; c += 2) {
-        mx0 = fmax3(mx0, __uint_as_float(r[0][c]), __uint_as_float(r[0][c + 1]));
-        mx1 = fmax3(mx1, __uint_as_float(r[1][c]), __uint_as_float(r[1][c + 1]));
-        mx2 = fmax3(mx2, __uint_as_float(r[2][c]), __uint_as_float(r[2][c + 1]));
-        mx3 = fmax3(mx3, __uint_as_float(r[3][c]), __uint_as_float(r[3][c + 1]));
-      }
-      const float m_tile = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
-      const float m_new = fmaxf(m_ref, m_tile);
-      const bool rescale = m_new > m_ref + kRescaleThreshold;
-      float alpha = 1.f;
-      if (rescale) {
-        // The reference max is kept integral (log2 units): partials over any split
-        // of the keys then differ by exact powers of two, so the bf16 rounding of P
-        // does not depend on the ring layout.
-        const float m_int = ceilf(m_new);
-        alpha = ex2_approx(m_ref - m_int);
-        l_sum *= alpha;
-        l_rnd *= alpha;
-        m_ref = m_int;
-      }
-      const float m_use = (m_ref == kNegInf) ? 0.f : m_ref;
       // Two row sums: of P (for the LSE) and of the bf16-rounded P that the PV MMA
       // consumes (to normalise O, so O stays an exact convex combination of V).
       // Scale-and-shift and the exact sum run on packed fp32 pairs; the rounded
       // sum adds the bf16 halves straight into fp32.
-      const uint64_t nm2 = f2_pack(-m_use, -m_use);
-      uint64_t ls_a = 0, ls_b = 0;
+      uint64_t nm2 = 0, ls_a = 0, ls_b = 0;
       float lr0 = 0.f, lr1 = 0.f, lr2 = 0.f, lr3 = 0.f;
       auto p_chunk = [&](int c) {
         uint32_t pk[16];
@@ -316,8 +292,62 @@ __global__ void __launch_bounds__(384, 1)
         }
         tmem_st16(tS + 16 * c, pk);
       };
-      p_chunk(0);
-      p_chunk(1);
+      // P = 2^(S log2e scale - m) for the whole tile, written over S in TMEM
+      auto p_tile = [&](float m_use) {
+        nm2 = f2_pack(-m_use, -m_use);
+        ls_a = ls_b = 0;
+        lr0 = lr1 = lr2 = lr3 = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) p_chunk(c);
+      };
+      auto tile_sum = [&]() {
+        float a0, a1, b0, b1;
+        f2_unpack(ls_a, a0, a1);
+        f2_unpack(ls_b, b0, b1);
+        return (a0 + a1) + (b0 + b1);
+      };
+      // First try the running reference max as it stands, without looking at
+      // this tile's max: that stands unless the tile's P would grow too large,
+      // which is rare once the first tile has set the reference.  Otherwise (and
+      // for a warp with a row that has seen no key yet) take the row max, move
+      // the reference when it grew past the threshold, and redo the tile.  One
+      // copy of the tile code serves both passes (instruction-cache footprint).
+      bool exact = __any_sync(0xffffffffu, m_ref == kNegInf);
+      bool rescale = false;
+      float alpha = 1.f;
+#pragma unroll 1
+      for (int pass = 0; pass < 2; ++pass) {
+        if (exact) {
+          // row max: eight independent chains of three-input max, eight deep
+          float mx[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) mx[k] = kNegInf;
+#pragma unroll
+          for (int i = 0; i < 16; i += 2)
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              mx[k] = fmax3(mx[k], __uint_as_float(r[k >> 1][16 * (k & 1) + i]),
+                            __uint_as_float(r[k >> 1][16 * (k & 1) + i + 1]));
+          const float m_tile =
+              fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(mx[3], mx[4], fmax3(mx[5], mx[6], mx[7]))) * sl2;
+          const float m_new = fmaxf(m_ref, m_tile);
+          rescale = m_new > m_ref + kRescaleThreshold;
+          if (rescale) {
+            // The reference max is kept integral (log2 units): partials over any
+            // split of the keys then differ by exact powers of two, so the bf16
+            // rounding of P does not depend on the ring layout.
+            const float m_int = ceilf(m_new);
+            alpha = ex2_approx(m_ref - m_int);
+            l_sum *= alpha;
+            l_rnd *= alpha;
+            m_ref = m_int;
+          }
+        }
+        p_tile((m_ref == kNegInf) ? 0.f : m_ref);
+        if (exact || !__any_sync(0xffffffffu, !(tile_sum() <= kSpecSumLimit))) break;
+        tmem_st_wait();  // the redo overwrites these P stores
+        exact = true;
+      }
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
         // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1)),
         // and must be rescaled before PV(j) adds to it.
@@ -332,18 +362,13 @@ __global__ void __launch_bounds__(384, 1)
           tmem_st32(tO + 32 * c, o);
         }
       }
+      // One arrival per warp: the shared-memory unit takes an mbarrier's
+      // arrivals one at a time, so 128 of them would hold the MMA issuer back.
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(b_p + 8 * qt);
-      p_chunk(2);
-      p_chunk(3);
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(b_p2 + 8 * qt);
-      float a0, a1, b0, b1;
-      f2_unpack(ls_a, a0, a1);
-      f2_unpack(ls_b, b0, b1);
-      l_sum += (a0 + a1) + (b0 + b1);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(b_p + 8 * qt);
+      l_sum += tile_sum();
       l_rnd += (lr0 + lr1) + (lr2 + lr3);
     }
     if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
