@@ -13,18 +13,23 @@
 // Warp roles (512 threads):
 //   warp 0       producer: K, V once; then Q_i with its LSE/Delta slices into a
 //                two-stage ring, and dO_i into a single buffer
-//   warp 1       TMEM owner + single-thread UMMA issuer
+//   warp 1       TMEM owner + single-thread UMMA issuer, per pair i:
+//                  [P_i written] dV_i, S_{i+1} | [dS_i written] dQ_i, dK_i |
+//                  [dQ_i read out] dP_{i+1}
+//                so the tensor pipe runs dV_i/S_{i+1} while the compute
+//                warpgroups work on dS_i, and dQ_i/dK_i while they work on P_{i+1}
 //   warps 4-11   two compute warpgroups, each on half of the 128 query columns
 //                (P^T, dS^T) and, at the end, half of the head dimension of dK/dV
 //   warps 12-15  dQ warpgroup: reads dQ_i out of tensor memory, stages it in its
 //                own shared-memory buffer and adds it into the accumulator with
 //                bulk reductions, off the compute warpgroups' path; every kChain
 //                pairs it also moves the dV/dK chain into the fp32 accumulators
-// Tensor memory: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dS^T/dQ after.
-// P^T and dS^T (bf16, two per column) overwrite columns [0,32) and [64,96) of
-// S^T and dP^T (each warpgroup packs into its own columns) and feed the dV and
-// dK MMAs from tensor memory; dS^T is also written to shared memory
-// (MN-major, 128-byte swizzle) as the A operand of the dQ MMA.
+// Tensor memory: dV [0,D), dK [D,2D), S^T/P^T [2D,2D+128), dP^T/dQ after.
+// P^T (bf16, two per column) overwrites columns [0,32) and [64,96) of S^T
+// (each warpgroup packs into its own columns) and feeds the dV MMA from tensor
+// memory.  dS^T goes to shared memory only (128 rows of key x 128 query
+// columns, two 64-column chunks, 128-byte swizzle): the same bytes are the
+// K-major A operand of dK = dS^T Q and the MN-major A operand of dQ = dS K.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
 
@@ -105,12 +110,14 @@ __global__ void __launch_bounds__(512, 1)
   const uint32_t b_doempty = smem_u32(bars + 6); // dO released (after dV_i)
   const uint32_t b_s = smem_u32(bars + 7);       // S^T_i in TMEM
   const uint32_t b_dp = smem_u32(bars + 8);      // dP^T_i in TMEM
-  const uint32_t b_pr = smem_u32(bars + 9);      // P^T, dS^T written (256 arrivals)
+  const uint32_t b_pr = smem_u32(bars + 9);      // dS^T_i written to shared memory
   const uint32_t b_dq = smem_u32(bars + 10);     // dQ_i in TMEM (and all earlier MMAs done)
-  const uint32_t b_dqf = smem_u32(bars + 11);    // dQ_i read out (128 arrivals)
+  const uint32_t b_dqf = smem_u32(bars + 11);    // dQ_i read out
   const uint32_t b_drain = smem_u32(bars + 12);
-  const uint32_t b_kvf = smem_u32(bars + 13);    // a finished dV/dK chain left tensor memory (128 arrivals)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 14);
+  const uint32_t b_kvf = smem_u32(bars + 13);    // a finished dV/dK chain left tensor memory
+  const uint32_t b_p = smem_u32(bars + 14);      // P^T_i packed in tensor memory
+  const uint32_t b_dsf = smem_u32(bars + 15);    // dQ_i and dK_i done: the dS buffer may be rewritten
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -136,6 +143,8 @@ __global__ void __launch_bounds__(512, 1)
     mbar_init(b_dqf, 4);
     mbar_init(b_drain, 1);
     mbar_init(b_kvf, 4);
+    mbar_init(b_p, 8);
+    mbar_init(b_dsf, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -195,9 +204,6 @@ __global__ void __launch_bounds__(512, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
-      // Per pair i: [dQ_{i-1} read out] dP_i | [P_i, dS_i written] dV_i,
-      // S_{i+1}, dK_i, dQ_i.  S_{i+1} goes right after dV_i (the last reader of
-      // P_i in the S region), so the next pair's P phase overlaps dK_i and dQ_i.
       auto issue_s = [&](int i) {  // S^T_i = K Q_i^T
         const uint32_t sq = sQ + (i & 1) * C::kTile;
 #pragma unroll
@@ -208,24 +214,7 @@ __global__ void __launch_bounds__(512, 1)
         }
         umma_commit(b_s);
       };
-      bool ok = mbar_wait(b_kv, 0, ab, 202);
-      if (ok && npairs > 0) {
-        ok = mbar_wait(b_qfull, 0, ab, 203);
-        if (ok) {
-          tc_fence_after();
-          issue_s(0);
-        }
-      }
-      for (int i = 0; i < npairs && ok; ++i) {
-        const int st = i & 1;
-        const uint32_t pi = i & 1;
-        const uint32_t sq = sQ + st * C::kTile;
-        // dP^T = V dO^T, once dQ_{i-1} has left this tensor-memory region
-        if (i > 0) {
-          if (!mbar_wait(b_dqf, pi ^ 1, ab, 204)) { ok = false; break; }
-        }
-        if (!mbar_wait(b_dofull, pi, ab, 207)) { ok = false; break; }
-        tc_fence_after();
+      auto issue_dp = [&]() {  // dP^T = V dO^T
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -233,35 +222,60 @@ __global__ void __launch_bounds__(512, 1)
                   kk > 0);
         }
         umma_commit(b_dp);
-        if (!mbar_wait(b_pr, pi, ab, 205)) { ok = false; break; }
+      };
+      bool ok = mbar_wait(b_kv, 0, ab, 202);
+      if (ok && npairs > 0) {
+        ok = mbar_wait(b_qfull, 0, ab, 203) && mbar_wait(b_dofull, 0, ab, 207);
+        if (ok) {
+          tc_fence_after();
+          issue_s(0);
+          issue_dp();
+        }
+      }
+      for (int i = 0; i < npairs && ok; ++i) {
+        const int st = i & 1;
+        const uint32_t pi = i & 1;
+        const uint32_t sq = sQ + st * C::kTile;
+        // dV += P^T dO once P_i is packed (A from tensor memory: query columns
+        // 0-63 in columns [0,32) of the S region, 64-127 in [64,96); B MN-major)
+        if (!mbar_wait(b_p, pi, ab, 205)) { ok = false; break; }
         if (i > 0 && i % C::kChain == 0) {  // the previous dV/dK chain has been flushed
           if (!mbar_wait(b_kvf, ((i / C::kChain) - 1) & 1, ab, 208)) { ok = false; break; }
         }
         tc_fence_after();
-        // dV += P^T dO   (A from tensor memory: packed query columns 0-63 in
-        // columns [0,32) of the S region, 64-127 in columns [64,96); B MN-major)
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8,
                   sdesc_sw128(sDO + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_doempty);
+        // S_{i+1} right behind dV_i, the last reader of P_i in the S region
         if (i + 1 < npairs) {
           if (!mbar_wait(b_qfull + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
           tc_fence_after();
           issue_s(i + 1);
         }
-        // dK += dS^T Q
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::tdK, tmem + C::tP + (kk >> 2) * 64 + (kk & 3) * 8,
-                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_qempty + 8 * st);
-        // dQ_i = dS K   (A = dS from shared memory, MN-major; B = K, MN-major)
+        // dQ_i = dS K and dK += dS^T Q, once dS_i is in shared memory (and the
+        // compute warpgroups have read dP_i, whose region dQ_i takes)
+        if (!mbar_wait(b_pr, pi, ab, 206)) { ok = false; break; }
+        tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           umma_ss(tmem + C::tP, sdesc_sw128(sDS + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
                   C::kIdescQ, kk > 0);
         umma_commit(b_dq);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_ss(tmem + C::tdK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(b_qempty + 8 * st);
+        umma_commit(b_dsf);
+        // dP_{i+1} once dQ_i has left the region and dO_{i+1} has landed
+        if (i + 1 < npairs) {
+          if (!mbar_wait(b_dqf, pi, ab, 204)) { ok = false; break; }
+          if (!mbar_wait(b_dofull, pi ^ 1, ab, 207)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp();
+        }
       }
       if (!ok) {  // let issued MMAs finish before tensor memory is released
         umma_commit(b_drain);
@@ -308,98 +322,109 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     };
-    bool ok = true;
-    for (int i = 0; i < npairs && ok; ++i) {
-      const int st = i & 1;
-      const uint32_t pi = i & 1;
+    // visible query columns c of pair i satisfy  qlo <= q0 + c < qe  and
+    // (causal) krow <= q0 + c
+    auto vis = [&](int i, bool& need_mask, int& cmin, int& cmax) {
       const int q0 = pl.start(i), qlo = pl.lo(i), qe = pl.end(i);
-      const float4* sl4 = reinterpret_cast<const float4*>(stat + st * 256);
-      const bool need_mask =
-          (it.k1 - it.k0 < 128) || (q0 + 128 > qe) || (q0 < qlo) || (p.causal && it.k1 - 1 > q0);
-      // visible query columns c satisfy  qlo <= q0 + c < qe  and (causal) krow <= q0 + c
-      const int cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
-      const int cmax = qe - q0;  // exclusive
-      // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64)
-      if (!wait_warp(b_s, pi, 210)) { ok = false; break; }
+      need_mask = (it.k1 - it.k0 < 128) || (q0 + 128 > qe) || (q0 < qlo) || (p.causal && it.k1 - 1 > q0);
+      cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
+      cmax = qe - q0;  // exclusive
+    };
+    uint32_t pk[32];  // P^T of the current pair, bf16 pairs (kept for its dS phase)
+    // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64),
+    // packed into this warpgroup's own columns of the S region (never into the
+    // other warpgroup's columns, which it may not have read yet)
+    auto p_phase = [&](int i) -> bool {
+      if (!wait_warp(b_s, i & 1, 210)) return false;
       tc_fence_after();
-      uint32_t pk[32];
-      {
-        uint32_t r[2][32];
-        tmem_ld32(tS + 64 * wg, r[0]);
-        tmem_ld32(tS + 64 * wg + 32, r[1]);
-        tmem_ld_wait();
-        reg_fence32(r[0]);
-        reg_fence32(r[1]);
+      bool need_mask;
+      int cmin, cmax;
+      vis(i, need_mask, cmin, cmax);
+      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i & 1) * 256);
+      uint32_t r[2][32];
+      tmem_ld32(tS + 64 * wg, r[0]);
+      tmem_ld32(tS + 64 * wg + 32, r[1]);
+      tmem_ld_wait();
+      reg_fence32(r[0]);
+      reg_fence32(r[1]);
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int c0 = 64 * wg + 32 * c + 2 * x;
-            const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
-            const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
-            float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x]), sl2, -la));
-            float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x + 1]), sl2, -lb));
-            if (need_mask) {
-              if (c0 < cmin || c0 >= cmax) p0 = 0.f;
-              if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
-            }
-            pk[16 * c + x] = pack_bf16x2(p0, p1);
+        for (int x = 0; x < 16; ++x) {
+          const int c0 = 64 * wg + 32 * c + 2 * x;
+          const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
+          const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
+          float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x]), sl2, -la));
+          float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x + 1]), sl2, -lb));
+          if (need_mask) {
+            if (c0 < cmin || c0 >= cmax) p0 = 0.f;
+            if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
           }
+          pk[16 * c + x] = pack_bf16x2(p0, p1);
         }
-        // packed P^T goes to the first half of this warpgroup's own 64 columns
-        // (never into the other warpgroup's columns, which it may not have read yet)
-        uint32_t w0[16], w1[16];
-#pragma unroll
-        for (int x = 0; x < 16; ++x) { w0[x] = pk[x]; w1[x] = pk[16 + x]; }
-        tmem_st16(tS + 64 * wg, w0);
-        tmem_st16(tS + 64 * wg + 16, w1);
       }
-      // ---- dS^T = scale P^T (dP^T - Delta)
-      if (!wait_warp(b_dp, pi, 211)) { ok = false; break; }
-      tc_fence_after();
-      {
-        uint32_t r[2][32];
-        tmem_ld32(tP + 64 * wg, r[0]);
-        tmem_ld32(tP + 64 * wg + 32, r[1]);
-        tmem_ld_wait();
-        reg_fence32(r[0]);
-        reg_fence32(r[1]);
-        uint32_t w[2][16];
+      uint32_t w0[16], w1[16];
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
-#pragma unroll
-          for (int x = 0; x < 16; ++x) {
-            const int c0 = 64 * wg + 32 * c + 2 * x;
-            const uint32_t pp = pk[16 * c + x];
-            const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
-            const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
-            const float d0 = bf16lo(pp) * (__uint_as_float(r[c][2 * x]) - da) * scale;
-            const float d1 = bf16hi(pp) * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
-            w[c][x] = pack_bf16x2(d0, d1);
-          }
-          tmem_st16(tP + 64 * wg + 16 * c, w[c]);
-        }
-        // dS^T to shared memory (this warpgroup's 64 query columns are chunk `wg`
-        // of the MN-major dS tile), once the dQ MMA of the previous pair has read it
-        if (i > 0 && !wait_warp(b_dq, pi ^ 1, 212)) { ok = false; break; }
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int pc = 0; pc < 4; ++pc) {
-            const int piece = c * 4 + pc;
-            asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((piece ^ (tid & 7)) << 4)),
-                         "r"(w[c][4 * pc]), "r"(w[c][4 * pc + 1]), "r"(w[c][4 * pc + 2]), "r"(w[c][4 * pc + 3])
-                         : "memory");
-          }
-      }
+      for (int x = 0; x < 16; ++x) { w0[x] = pk[x]; w1[x] = pk[16 + x]; }
+      tmem_st16(tS + 64 * wg, w0);
+      tmem_st16(tS + 64 * wg + 16, w1);
       tmem_st_wait();
-      fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
+      if (lane == 0) mbar_arrive(b_p);
+      return true;
+    };
+    // ---- dS^T = scale P^T (dP^T - Delta), to shared memory (this warpgroup's
+    // 64 query columns are chunk `wg`) once dQ_{i-1} and dK_{i-1} have read the
+    // previous one
+    auto ds_phase = [&](int i) -> bool {
+      if (!wait_warp(b_dp, i & 1, 211)) return false;
+      tc_fence_after();
+      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i & 1) * 256);
+      uint32_t r[2][32];
+      tmem_ld32(tP + 64 * wg, r[0]);
+      tmem_ld32(tP + 64 * wg + 32, r[1]);
+      tmem_ld_wait();
+      reg_fence32(r[0]);
+      reg_fence32(r[1]);
+      uint32_t w[2][16];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+#pragma unroll
+        for (int x = 0; x < 16; ++x) {
+          const int c0 = 64 * wg + 32 * c + 2 * x;
+          const uint32_t pp = pk[16 * c + x];
+          const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
+          const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
+          const float d0 = bf16lo(pp) * (__uint_as_float(r[c][2 * x]) - da) * scale;
+          const float d1 = bf16hi(pp) * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
+          w[c][x] = pack_bf16x2(d0, d1);
+        }
+      }
+      // dP_i is in registers: its tensor-memory region may take dQ_i
+      tc_fence_before();
+      if (i > 0 && !wait_warp(b_dsf, (i - 1) & 1, 212)) return false;
+#pragma unroll
+      for (int c = 0; c < 2; ++c)
+#pragma unroll
+        for (int pc = 0; pc < 4; ++pc) {
+          const int piece = c * 4 + pc;
+          asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((piece ^ (tid & 7)) << 4)),
+                       "r"(w[c][4 * pc]), "r"(w[c][4 * pc + 1]), "r"(w[c][4 * pc + 2]), "r"(w[c][4 * pc + 3])
+                       : "memory");
+        }
+      fence_proxy_async_smem();
+      __syncwarp();
       if (lane == 0) mbar_arrive(b_pr);
+      return true;
+    };
+    bool ok = npairs == 0 || p_phase(0);
+    for (int i = 0; i < npairs && ok; ++i) {
+      ok = ds_phase(i);
+      if (ok && i + 1 < npairs) ok = p_phase(i + 1);
     }
-    // every MMA of the CTA is done once the last dQ has landed
-    if (ok && npairs > 0 && wait_warp(b_dq, (npairs - 1) & 1, 213)) {
+    // every MMA of the CTA is done once dQ and dK of the last pair are
+    if (ok && npairs > 0 && wait_warp(b_dsf, (npairs - 1) & 1, 213)) {
       tc_fence_after();
       flush_dkdv();
     }
@@ -456,6 +481,8 @@ __global__ void __launch_bounds__(512, 1)
       // and more pairs follow: add the chain into the fp32 accumulators, so the
       // MMA can restart the chain in tensor memory.  Here lanes = key rows.
       if ((j + 1) % C::kChain == 0 && j + 1 < npairs) {
+        if (!wait_warp(b_dsf, j & 1, 221)) break;  // dK_j (issued after dQ_j) is done too
+        tc_fence_after();
         const int krow = it.k0 + tid;
         const bool valid = krow < it.k1;
 #pragma unroll
