@@ -377,12 +377,36 @@ def main():
     chk(lib.ra_workspace_status(P_(ws_f), sp))
     chk(lib.ra_workspace_status(P_(ws_b), sp))
 
+    # ---------------------------------------------------------------- single-launch forward
+    # The same forward with the whole ring in one launch (ra_fwd_fused): timed
+    # after the ring-step region, on its own output buffers.
+    fused = None
+    wfu = plan.fused_workspace_bytes()
+    ws_u = torch.empty(wfu, dtype=torch.uint8, device=dev)
+    o_u = torch.empty_like(o)
+    lse_u = torch.empty_like(lse)
+    for _ in range(max(1, args.warmup)):
+        chk(lib.ra_fwd_fused(H, P_(q), P_(k), P_(v), P_(o_u), 0, P_(lse_u), P_(ws_u), wfu, sp))
+    torch.cuda.synchronize()
+    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    u0.record(stream)
+    for _ in range(args.steps):
+        chk(lib.ra_fwd_fused(H, P_(q), P_(k), P_(v), P_(o_u), 0, P_(lse_u), P_(ws_u), wfu, sp))
+    u1.record(stream)
+    torch.cuda.synchronize()
+    chk(lib.ra_workspace_status(P_(ws_u), sp))
+    fused_ms = max_over_ranks(u0.elapsed_time(u1), dist, dev) / args.steps
+
     ff, fb = useful_flops(wl)
     ms_step = ms_total / args.steps
     value = whole_job_tflops(world, ff + fb, args.steps, ms_total)
     peak_b, peak_s, hbm, peak_kind = peaks()
     fwd_ms = sum(t_f) / args.steps
     bwd_ms = sum(t_b) / args.steps
+    fused = {"fwd_ms": fused_ms, "fwd_tflops": ff / (fused_ms * 1e-3) / 1e12,
+             "fwd_plus_ring_step_bwd_tflops": world * (ff + fb) / ((fused_ms + bwd_ms) * 1e-3) / 1e12,
+             "note": "forward with the whole ring in one launch (running state kept on chip); "
+                     "timed separately, not part of value"}
 
     # roofline of the dominant kernel (per-launch events on the launching stream)
     if sum(t_b) >= sum(t_f):
@@ -446,7 +470,7 @@ def main():
             "fwd_tflops": ff / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
             "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
             "useful_flops_per_step": ff + fb, "strict_bwd_flops_per_step": 0.8 * fb,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "single_launch_forward": fused,
             "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3),
             "clocks": clk.summary(),
         }

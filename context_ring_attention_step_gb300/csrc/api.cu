@@ -30,6 +30,11 @@ struct ra_plan {
   std::vector<int64_t> fwd_off;  // steps + 1
   std::vector<BwdItem> bwd;
   std::vector<int64_t> bwd_off;  // steps + 1
+  // single-launch forward over all ring steps: items (kb0 = first tile, ke0 =
+  // tile count, kb1/ke1 = active tiles of the two 128-row query tiles) and the
+  // key tiles, (start, range end) per tile, ring step by ring step
+  std::vector<FwdItem> ffw;
+  std::vector<int32_t> ftiles;
   int64_t visible_pairs = 0;
 };
 
@@ -150,12 +155,71 @@ void build_items(ra_plan& P) {
   }
 }
 
+// Work list of the single-launch forward: one item per 256-row query chunk,
+// holding every key tile the chunk meets over the whole ring, in ring order
+// (step s: the key/value shard (r - s) mod cp, its ranges in ascending order),
+// causally clipped to keys < q1.  The running (O, LSE) of the chunk then stays
+// on chip from the first ring step to the last: each step's partial is merged
+// by continuing the online softmax instead of through HBM.
+void build_fused(ra_plan& P) {
+  P.ffw.clear();
+  P.ftiles.clear();
+  for (int32_t d = 0; d < P.num_docs; ++d) {
+    const int32_t base = P.cu[d], L = P.cu[d + 1] - P.cu[d], cp = P.cp[d];
+    if (L == 0) continue;
+    for (int32_t r = 0; r < cp; ++r) {
+      int32_t qb[2], qe[2];
+      const int nq = shard(L, cp, P.layout, r, qb, qe);
+      for (int a = 0; a < nq; ++a) {
+        for (int32_t q0 = base + qb[a]; q0 < base + qe[a]; q0 += 256) {
+          const int32_t q1 = std::min(q0 + 256, base + qe[a]);
+          const int32_t last0 = std::min(q0 + 128, q1) - 1, last1 = q1 - 1;
+          const bool two = q0 + 128 < q1;
+          FwdItem it{};
+          it.q0 = q0;
+          it.q1 = q1;
+          it.kb0 = (int32_t)(P.ftiles.size() / 2);
+          int32_t n = 0, na0 = 0, na1 = 0;
+          for (int32_t s = 0; s < cp; ++s) {
+            const int32_t j = ((r - s) % cp + cp) % cp;
+            int32_t kb[2], ke[2];
+            const int nk = shard(L, cp, P.layout, j, kb, ke);
+            for (int c = 0; c < nk; ++c) {
+              const int32_t b = base + kb[c];
+              const int32_t e = P.causal ? std::min(base + ke[c], q1) : base + ke[c];
+              for (int32_t kst = b; kst < e; kst += 128) {
+                P.ftiles.push_back(kst);
+                P.ftiles.push_back(e);
+                ++n;
+                if (!P.causal || kst <= last0) ++na0;
+                if (two && (!P.causal || kst <= last1)) ++na1;
+              }
+            }
+          }
+          if (n == 0) continue;
+          it.ke0 = n;
+          it.kb1 = na0;
+          it.ke1 = na1;
+          it.flags = ra::kFirstStep;
+          it.tiles = n;
+          P.ffw.push_back(it);
+        }
+      }
+    }
+  }
+  // longest first: the grid's tail is short
+  std::stable_sort(P.ffw.begin(), P.ffw.end(), [](const FwdItem& a, const FwdItem& b) { return a.tiles > b.tiles; });
+}
+
 // Row pitch (in floats) of the backward's per-head Delta and LSE*log2(e)
 // rows: T rounded up to 4, so every row starts 16-byte aligned for TMA.
 int64_t stat_pitch(const ra_plan& P) { return ((int64_t)P.T + 3) & ~int64_t(3); }
 
 struct FwdLayout {
   size_t items, orun, total;
+};
+struct FusedLayout {
+  size_t items, tiles, total;
 };
 struct BwdLayout {
   size_t items, delta, lse2, dq, dk, dv, total;
@@ -168,6 +232,17 @@ FwdLayout fwd_layout(const ra_plan& P, int o_fp32) {
   off = align256(off + P.fwd.size() * sizeof(FwdItem));
   l.orun = off;
   if (!o_fp32) off = align256(off + (size_t)P.T * P.Hq * P.D * 4);
+  l.total = off;
+  return l;
+}
+
+FusedLayout fused_layout(const ra_plan& P) {
+  FusedLayout l{};
+  size_t off = kHeader;
+  l.items = off;
+  off = align256(off + P.ffw.size() * sizeof(FwdItem));
+  l.tiles = off;
+  off = align256(off + P.ftiles.size() * sizeof(int32_t));
   l.total = off;
   return l;
 }
@@ -320,6 +395,7 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
     P->visible_pairs += causal ? L * (L + 1) / 2 : L * L;
   }
   build_items(*P);
+  build_fused(*P);
   *out = P;
   return RA_OK;
 }
@@ -463,6 +539,71 @@ ra_status ra_fwd(const ra_plan* P, const void* q, const void* k, const void* v, 
     rs = ra_fwd_ring_step(P, s, q, k, v, o, o_is_fp32, lse, workspace, workspace_bytes, stream);
   if (rs == RA_OK) rs = ra_fwd_finish(P, o, o_is_fp32, workspace, workspace_bytes, stream);
   return rs;
+}
+
+// ---------------------------------------------------------------- forward, one launch
+
+ra_status ra_plan_fused_workspace_bytes(const ra_plan* P, size_t* fwd_bytes) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  if (!fwd_bytes) return fail(RA_ERR_INVALID_ARG, "fwd_bytes is NULL");
+  *fwd_bytes = fused_layout(*P).total;
+  return RA_OK;
+}
+
+ra_status ra_plan_fused_items(const ra_plan* P, int32_t* items, int64_t item_capacity, int32_t* tiles,
+                              int64_t tile_capacity, int64_t* num_items, int64_t* num_tiles) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  const int64_t ni = (int64_t)P->ffw.size(), nt = (int64_t)P->ftiles.size() / 2;
+  if (num_items) *num_items = ni;
+  if (num_tiles) *num_tiles = nt;
+  if (items) {
+    if (item_capacity < ni) return fail(RA_ERR_INVALID_ARG, "item capacity %lld < %lld", (long long)item_capacity, (long long)ni);
+    if (ni) std::memcpy(items, P->ffw.data(), (size_t)ni * sizeof(FwdItem));
+  }
+  if (tiles) {
+    if (tile_capacity < nt) return fail(RA_ERR_INVALID_ARG, "tile capacity %lld < %lld", (long long)tile_capacity, (long long)nt);
+    if (nt) std::memcpy(tiles, P->ftiles.data(), (size_t)nt * 2 * sizeof(int32_t));
+  }
+  return RA_OK;
+}
+
+ra_status ra_fwd_fused(const ra_plan* P, const void* q, const void* k, const void* v, void* o, int32_t o_is_fp32,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
+    return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
+  const FusedLayout L = fused_layout(*P);
+  if (workspace_bytes < L.total)
+    return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, L.total);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+  uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  if (P->ffw.empty()) return RA_OK;
+  e = cudaMemcpyAsync(ws + L.items, P->ffw.data(), P->ffw.size() * sizeof(FwdItem), cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess)
+    e = cudaMemcpyAsync(ws + L.tiles, P->ftiles.data(), P->ftiles.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
+  if (e != cudaSuccess) return cuda_fail(e, "work-list copy");
+  CUtensorMap tq, tk, tv;
+  if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
+      !encode_thd(&tv, v, P->T, P->Hkv, P->D))
+    return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
+  ra::FwdParams p{};
+  p.items = reinterpret_cast<const FwdItem*>(ws + L.items);
+  p.tiles = reinterpret_cast<const int2*>(ws + L.tiles);
+  p.Hq = P->Hq;
+  p.Hkv = P->Hkv;
+  p.T = P->T;
+  p.causal = P->causal;
+  p.scale_log2 = P->scale * 1.4426950408889634f;
+  p.o_out = o;
+  p.o_bf16 = o_is_fp32 ? 0 : 1;
+  p.lse = lse;
+  p.status = reinterpret_cast<int*>(ws);
+  e = ra::launch_fwd_fused(P->D, tq, tk, tv, p, (int)P->ffw.size(), st);
+  if (e != cudaSuccess) return cuda_fail(e, "fused forward launch");
+  return RA_OK;
 }
 
 // ---------------------------------------------------------------- backward

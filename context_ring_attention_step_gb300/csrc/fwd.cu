@@ -45,15 +45,26 @@ struct FwdCfg {
   static constexpr uint32_t kIdescPV = idesc_bf16_f32(128, D, false, true);
 };
 
+// Key tiles of one CTA.  Ring-step launch: up to two sorted key ranges, cut
+// into 128-key tiles.  Single launch over the ring: an explicit table of
+// (tile start, range end), ring step by ring step.
+template <bool kFused>
 struct TileList {
   int32_t kb0, ke0, kb1, ke1, n0, n;
-  __device__ __forceinline__ int start(int j) const { return j < n0 ? kb0 + 128 * j : kb1 + 128 * (j - n0); }
-  __device__ __forceinline__ int end(int j) const { return j < n0 ? ke0 : ke1; }
+  const int2* tab;
+  __device__ __forceinline__ int start(int j) const {
+    if constexpr (kFused) return tab[j].x;
+    else return j < n0 ? kb0 + 128 * j : kb1 + 128 * (j - n0);
+  }
+  __device__ __forceinline__ int end(int j) const {
+    if constexpr (kFused) return tab[j].y;
+    else return j < n0 ? ke0 : ke1;
+  }
 };
 
 __device__ __forceinline__ int ceil128(int a, int b) { return b > a ? (b - a + 127) / 128 : 0; }
 
-template <int D>
+template <int D, bool kFused>
 __global__ void __launch_bounds__(384, 1)
     ring_fwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -80,25 +91,42 @@ __global__ void __launch_bounds__(384, 1)
   const int g = h / (p.Hq / p.Hkv);
   const FwdItem it = p.items[blockIdx.x / p.Hq];
 
-  TileList tl;
-  tl.kb0 = it.kb0; tl.ke0 = it.ke0; tl.kb1 = it.kb1; tl.ke1 = it.ke1;
-  tl.n0 = ceil128(it.kb0, it.ke0);
-  tl.n = tl.n0 + ceil128(it.kb1, it.ke1);
-  // active key tiles of each Q tile form a prefix of the tile list
-  int n_act[2];
+  TileList<kFused> tl;
+  int n_act[2];   // key tiles each Q tile sees
   bool q_act[2];
+  int last_row[2];
 #pragma unroll
   for (int qt = 0; qt < 2; ++qt) {
     const int first = it.q0 + 128 * qt;
     q_act[qt] = first < it.q1;
-    const int last = min(first + 128, it.q1) - 1;
-    int n = 0;
-    if (q_act[qt]) {
-      if (!p.causal) n = tl.n;
-      else while (n < tl.n && tl.start(n) <= last) ++n;
-    }
-    n_act[qt] = n;
+    last_row[qt] = min(first + 128, it.q1) - 1;
   }
+  if constexpr (kFused) {
+    tl.tab = p.tiles + it.kb0;
+    tl.n = it.ke0;
+    n_act[0] = q_act[0] ? it.kb1 : 0;
+    n_act[1] = q_act[1] ? it.ke1 : 0;
+  } else {
+    tl.kb0 = it.kb0; tl.ke0 = it.ke0; tl.kb1 = it.kb1; tl.ke1 = it.ke1;
+    tl.n0 = ceil128(it.kb0, it.ke0);
+    tl.n = tl.n0 + ceil128(it.kb1, it.ke1);
+    // here the active key tiles of each Q tile form a prefix of the tile list
+#pragma unroll
+    for (int qt = 0; qt < 2; ++qt) {
+      int n = 0;
+      if (q_act[qt]) {
+        if (!p.causal) n = tl.n;
+        else while (n < tl.n && tl.start(n) <= last_row[qt]) ++n;
+      }
+      n_act[qt] = n;
+    }
+  }
+  // does a Q tile (in scalars, so the arrays above stay in registers) see key
+  // tile j; causal: a tile that starts after its last row is skipped
+  auto active = [&](int j, bool qa, int last, int na) -> bool {
+    if constexpr (kFused) return qa && (!p.causal || tl.start(j) <= last);
+    else return j < na;
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(b_q, 1);
@@ -169,6 +197,9 @@ __global__ void __launch_bounds__(384, 1)
     const int qt = warp - 1;
     if (lane == 0) {
       const int na = qt == 0 ? n_act[0] : n_act[1];
+      const bool my_qa = qt == 0 ? q_act[0] : q_act[1];
+      const int my_last = qt == 0 ? last_row[0] : last_row[1];
+      auto act = [&](int j) { return active(j, my_qa, my_last, na); };
       const uint32_t tS = tmem + qt * 128, tO = tmem + 256 + qt * D, qa = sQ + qt * C::kTile;
       bool ok = mbar_wait(b_q, 0, ab, 102);
       tc_fence_after();
@@ -183,20 +214,24 @@ __global__ void __launch_bounds__(384, 1)
           umma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), C::kIdescQK, kk > 0);
         }
       };
+      // b_s is committed right after each QK of a tile this Q tile sees (S
+      // ready; it also covers the P.V before it), and once more after the last
+      // P.V (O final)
       if (ok) ok = mbar_wait(b_full + 8 * stage, kph, ab, 103);
       if (ok) {
         tc_fence_after();
-        if (na > 0) { qk(stage); umma_commit(b_s + 8 * qt); }
+        if (act(0)) { qk(stage); umma_commit(b_s + 8 * qt); }
         umma_commit(b_empty + 8 * stage);
         advance();
       }
       uint32_t pph = 0;
+      int u = 0;  // P.V issued so far
       for (int j = 0; j < tl.n && ok; ++j) {
         const int vst = stage;
         if (!mbar_wait(b_full + 8 * vst, kph, ab, 104)) { ok = false; break; }
         tc_fence_after();
         advance();  // stage now holds K_{j+1}
-        if (j < na) {
+        if (act(j)) {
           if (!mbar_wait(b_p + 8 * qt, pph, ab, 105)) { ok = false; break; }
           pph ^= 1;
           tc_fence_after();
@@ -204,17 +239,17 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
             umma_ts(tO, tS + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), C::kIdescPV,
-                    (j > 0 || kk > 0) ? 1u : 0u);
+                    (u > 0 || kk > 0) ? 1u : 0u);
+          if (++u == na) umma_commit(b_s + 8 * qt);  // O final
         }
         umma_commit(b_empty + 8 * vst);  // V_j: free once this tile's P.V has run
         if (j + 1 < tl.n) {
           if (!mbar_wait(b_full + 8 * stage, kph, ab, 106)) { ok = false; break; }
           tc_fence_after();
-          if (j + 1 < na) qk(stage);
+          if (act(j + 1)) { qk(stage); umma_commit(b_s + 8 * qt); }  // S(j+1) ready
           umma_commit(b_empty + 8 * stage);  // K_{j+1}: free once this tile's QK has run
           advance();
         }
-        if (j < na) umma_commit(b_s + 8 * qt);  // S(j+1) ready, or O final after the last tile
       }
       if (!ok) {  // let issued MMAs finish before tensor memory is released
         umma_commit(b_drain + 8 * qt);
@@ -240,7 +275,10 @@ __global__ void __launch_bounds__(384, 1)
     const int na = qt == 0 ? n_act[0] : n_act[1];
     const bool qa = qt == 0 ? q_act[0] : q_act[1];
     const int na_other = qt == 0 ? n_act[1] : n_act[0];
-    for (int j = 0; j < na; ++j) {
+    const int my_last = qt == 0 ? last_row[0] : last_row[1];
+    int u = 0;  // tiles done so far
+    for (int j = 0; j < tl.n; ++j) {
+      if (!active(j, qa, my_last, na)) continue;
       if (!mbar_wait(b_s + 8 * qt, sph, ab, 110)) { ok = false; break; }
       sph ^= 1;
       tc_fence_after();
@@ -252,7 +290,7 @@ __global__ void __launch_bounds__(384, 1)
       // The two softmax warpgroups take turns (Q0 tile j after Q1 tile j-1, Q1
       // tile j after Q0 tile j): each then runs alone on the SM's schedulers,
       // and their MMAs reach the tensor pipe interleaved instead of together.
-      const int k_other = j - (qt == 0 ? 1 : 0);
+      const int k_other = u - (qt == 0 ? 1 : 0);
       const bool turn = k_other < 0 || k_other >= na_other ||
                         mbar_wait(b_p + 8 * (1 - qt), (uint32_t)k_other & 1u, ab, 112);
       tmem_ld_wait();
@@ -348,9 +386,9 @@ __global__ void __launch_bounds__(384, 1)
         tmem_st_wait();  // the redo overwrites these P stores
         exact = true;
       }
-      if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds PV of tiles < j (complete: S(j) was committed after PV(j-1)),
-        // and must be rescaled before PV(j) adds to it.
+      if (u > 0 && __any_sync(0xffffffffu, rescale)) {
+        // O holds PV of the tiles before (complete: this S was committed after
+        // their P.V), and must be rescaled before this tile's P.V adds to it.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -370,13 +408,52 @@ __global__ void __launch_bounds__(384, 1)
       if (lane == 0) mbar_arrive(b_p + 8 * qt);
       l_sum += tile_sum();
       l_rnd += (lr0 + lr1) + (lr2 + lr3);
+      ++u;
     }
     if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
       if (na > 0) {
         ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
         tc_fence_after();
       }
-      if (ok) {
+      if (ok && kFused) {
+        // the whole ring is done: O = (sum of P V) / (sum of the bf16 P), final LSE
+        const bool valid = row < it.q1;
+        const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
+        const float inv_l = (l_rnd > 0.f) ? 1.f / l_rnd : 0.f;
+        if (valid) p.lse[(size_t)h * p.T + row] = lse_b;
+        const size_t obase = ((size_t)row * p.Hq + h) * D;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          if (na > 0) {
+            tmem_ld32(tO + 32 * c, o);
+            tmem_ld_wait();
+            reg_fence32(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
+          if (!valid) continue;
+          if (p.o_bf16) {
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o_out) + obase + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              uint4 w;
+              w.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
+              w.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
+              w.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
+              w.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
+              dst[i] = w;
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o_out) + obase + 32 * c);
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
+                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+          }
+        }
+      } else if (ok) {
         const bool valid = row < it.q1;
         const bool first = (it.flags & kFirstStep) != 0;
         const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
@@ -442,10 +519,10 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-template <int D>
+template <int D, bool kFused>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                    int num_items, cudaStream_t stream) {
-  auto kern = ring_fwd_step_kernel<D>;
+  auto kern = ring_fwd_step_kernel<D, kFused>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items * p.Hq;
@@ -458,8 +535,15 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
 
 cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                             const FwdParams& p, int num_items, cudaStream_t stream) {
-  if (head_dim == 128) return launch<128>(tq, tk, tv, p, num_items, stream);
-  if (head_dim == 64) return launch<64>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 128) return launch<128, false>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 64) return launch<64, false>(tq, tk, tv, p, num_items, stream);
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_fwd_fused(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdParams& p, int num_items, cudaStream_t stream) {
+  if (head_dim == 128) return launch<128, true>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 64) return launch<64, true>(tq, tk, tv, p, num_items, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -43,9 +43,14 @@ struct FwdParams {
   const FwdItem* items;
   int32_t Hq, Hkv, T, causal;
   float scale_log2;  // softmax scale * log2(e)
-  float* o_run;      // fp32 [T, Hq, D] running (normalised) output
+  float* o_run;      // fp32 [T, Hq, D] running (normalised) output (ring-step launches)
   float* lse;        // fp32 [Hq, T] running log-sum-exp (natural log)
   int* status;       // workspace status word
+  // single launch over all ring steps: per-tile (start, range end) table and
+  // the final output, written once (bf16 or fp32)
+  const int2* tiles;
+  void* o_out;
+  int32_t o_bf16;
 };
 
 struct BwdParams {
@@ -66,6 +71,8 @@ struct BwdParams {
 ra_status set_last_error(ra_status st, const char* msg);
 
 // Kernel launch wrappers (return the launch error).
+cudaError_t launch_fwd_fused(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                             const FwdParams& p, int num_items, cudaStream_t stream);
 cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, int num_items,
                             cudaStream_t stream);

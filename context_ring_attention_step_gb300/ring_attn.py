@@ -71,6 +71,12 @@ def load_library(path: str | None = None):
     for name in ("ra_fwd_prepare", "ra_fwd_ring_step", "ra_fwd_finish", "ra_bwd_prepare", "ra_bwd_ring_step",
                  "ra_bwd_finish"):
         getattr(lib, name).restype = i32
+    lib.ra_fwd_fused.argtypes = [P, P, P, P, P, i32, P, P, sz, P]
+    lib.ra_fwd_fused.restype = i32
+    lib.ra_plan_fused_workspace_bytes.argtypes = [P, c.POINTER(sz)]
+    lib.ra_plan_fused_workspace_bytes.restype = i32
+    lib.ra_plan_fused_items.argtypes = [P, c.POINTER(i32), i64, c.POINTER(i32), i64, c.POINTER(i64), c.POINTER(i64)]
+    lib.ra_plan_fused_items.restype = i32
     lib.ra_workspace_status.argtypes = [P, P]
     lib.ra_workspace_status.restype = i32
     _lib = lib
@@ -145,6 +151,23 @@ class Plan:
         items = [tuple(buf[8 * i:8 * i + 8]) for i in range(n.value)]
         return items, list(off)
 
+    def fused_workspace_bytes(self):
+        """Workspace bytes of the single-launch forward."""
+        f = ctypes.c_size_t()
+        _check(_lib.ra_plan_fused_workspace_bytes(self._handle, ctypes.byref(f)))
+        return f.value
+
+    def fused_items(self):
+        """(items as 8-int tuples, tiles as (start, range end) pairs) of the single-launch forward."""
+        ni, nt = ctypes.c_int64(), ctypes.c_int64()
+        _check(_lib.ra_plan_fused_items(self._handle, None, 0, None, 0, ctypes.byref(ni), ctypes.byref(nt)))
+        ib = (ctypes.c_int32 * max(1, 8 * ni.value))()
+        tb = (ctypes.c_int32 * max(1, 2 * nt.value))()
+        _check(_lib.ra_plan_fused_items(self._handle, ib, ni.value, tb, nt.value, ctypes.byref(ni),
+                                        ctypes.byref(nt)))
+        return [tuple(ib[8 * i:8 * i + 8]) for i in range(ni.value)], [tuple(tb[2 * i:2 * i + 2])
+                                                                      for i in range(nt.value)]
+
     def shard_token_ranges(self, doc, rank):
         b, e, n = (ctypes.c_int32 * 2)(), (ctypes.c_int32 * 2)(), ctypes.c_int32()
         _check(_lib.ra_shard_token_ranges(self._handle, int(doc), int(rank), b, e, ctypes.byref(n)))
@@ -171,10 +194,12 @@ def _check_tensor(name, t, shape, dtype):
 
 
 def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, scale=None,
-                  o_fp32=False, plan=None, workspace=None, check=False):
+                  o_fp32=False, plan=None, workspace=None, check=False, fused=False):
     """Ring attention forward: returns (o [T,Hq,d], lse [Hq,T] fp32).
 
-    ``check=True`` synchronises and raises if a kernel reported a timeout.
+    ``fused=True`` runs the whole ring in one launch (ra_fwd_fused) instead of
+    one launch per ring step.  ``check=True`` synchronises and raises if a
+    kernel reported a timeout.
     """
     T, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -186,11 +211,12 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, sc
     dev = q.device
     o = torch.empty((T, Hq, D), dtype=torch.float32 if o_fp32 else torch.bfloat16, device=dev)
     lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
-    ws_bytes = plan.workspace_bytes(o_fp32=o_fp32)[0]
+    ws_bytes = plan.fused_workspace_bytes() if fused else plan.workspace_bytes(o_fp32=o_fp32)[0]
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    _check(_lib.ra_fwd(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), int(o_fp32), _ptr(lse),
-                       _ptr(workspace), workspace.numel(), _stream(dev)))
+    call = _lib.ra_fwd_fused if fused else _lib.ra_fwd
+    _check(call(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), int(o_fp32), _ptr(lse),
+                _ptr(workspace), workspace.numel(), _stream(dev)))
     if check:
         _check(workspace_status(workspace, dev))
     return o, lse

@@ -143,6 +143,38 @@ ra_status ra_shard_token_ranges(const ra_plan* plan, int32_t doc, int32_t rank,
                                 int32_t* begin2, int32_t* end2, int32_t* count);
 
 /*
+ * Forward in one launch over the whole ring (same result as ra_fwd).  Each
+ * CTA keeps one 256-row query chunk's running (O, row max, row sums) on chip
+ * and visits the key/value shards in ring order, s = 0 .. cp-1 (shard
+ * (r - s) mod cp): the merge of step s into the running state is the online
+ * softmax continuing over that shard's key tiles (NVSHMEM/XLA page,
+ * "Paralelismo de contexto y atencion en anillo": attention is accumulated
+ * incrementally as the KV blocks circulate; Accelerate guide, "Detalhes
+ * tecnicos": `combine` of the per-shard results), so no running output goes
+ * through HBM between steps and O is written once, in its final dtype.
+ * Arguments as ra_fwd; workspace: device, >= ra_plan_fused_workspace_bytes.
+ * The caller owns every buffer; errors as ra_fwd (RA_ERR_WORKSPACE when the
+ * workspace is too small).
+ */
+ra_status ra_fwd_fused(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
+                       int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of ra_fwd_fused (header, work list, key-tile table). */
+ra_status ra_plan_fused_workspace_bytes(const ra_plan* plan, size_t* fwd_bytes);
+
+/*
+ * The single-launch forward's work list, for inspection and tests: items as
+ * int32[8] each {q0, q1, first tile, tile count, active tiles of rows
+ * [q0, q0+128), active tiles of rows [q0+128, q1), flags, tile count}, and
+ * tiles as int32[2] each {tile start, end of its key range} (the tile covers
+ * [start, min(start + 128, end))), ring step by ring step.  Either output may
+ * be NULL; *num_items / *num_tiles receive the sizes; RA_ERR_INVALID_ARG if a
+ * capacity is too small for a non-NULL output.
+ */
+ra_status ra_plan_fused_items(const ra_plan* plan, int32_t* items, int64_t item_capacity, int32_t* tiles,
+                              int64_t tile_capacity, int64_t* num_items, int64_t* num_tiles);
+
+/*
  * Forward: for s = 0 .. steps-1 every query shard r attends to key/value
  * shard (r - s) mod cp of its document (one kernel launch per ring step,
  * tcgen05 tensor-core block attention with online softmax); each step's

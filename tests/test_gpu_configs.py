@@ -129,3 +129,30 @@ def test_ring_equals_cp1_at_128k(ra):
                            grads_fp32=True, plan=plan16, check=True)
     for name, a, b in zip(("dq", "dk", "dv"), g16, g1):
         assert (a - b).abs().max().item() <= RING_TOL, name
+
+
+def test_fused_forward_at_128k(ra):
+    """Single-launch forward at 128K: equals the ring-step forward within 1e-3
+    (fp32 outputs, full tensors) and the oracle on sampled rows (bf16 output)."""
+    wl = workload("long_128k")
+    qh, kh, vh, _ = _inputs(wl)
+    q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
+    cps = list(wl.cp_per_doc)
+    plan = ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    o1, l1 = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, cps, wl.layout, True, wl.softmax_scale, o_fp32=True,
+                              plan=plan, check=True)
+    o2, l2 = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, cps, wl.layout, True, wl.softmax_scale, o_fp32=True,
+                              plan=plan, check=True, fused=True)
+    assert (o1 - o2).abs().max().item() <= RING_TOL
+    assert (l1 - l2).abs().max().item() <= RING_TOL
+    del o1, l1, o2, l2
+    o, lse = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, cps, wl.layout, True, wl.softmax_scale, plan=plan,
+                              check=True, fused=True)
+    o, lse = o.float().cpu().numpy(), lse.cpu().numpy()
+    rng = np.random.default_rng(7)
+    for h in (3, 28):
+        rows = _sample_rows(wl, rng, 16)
+        qs, ks, vs = qh[:, h:h + 1].contiguous(), kh[:, h // 4:h // 4 + 1].contiguous(), vh[:, h // 4:h // 4 + 1].contiguous()
+        ro, rl = A.attention_rows(qs, ks, vs, wl.cu_seqlens, rows, 0, True, wl.softmax_scale)
+        assert (np.abs(o[rows, h] - ro) - (O_TOL + np.abs(ro) * 2.0 ** -9)).max() <= 0
+        assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL

@@ -28,20 +28,20 @@ def ra():
     return m
 
 
-def _run_fwd(ra, wl, q, k, v, o_fp32=False, cp=None, layout=None):
+def _run_fwd(ra, wl, q, k, v, o_fp32=False, cp=None, layout=None, fused=False):
     cps = list(wl.cp_per_doc) if cp is None else cp
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
     o, lse = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, layout or wl.layout, wl.causal,
-                              wl.softmax_scale, o_fp32=o_fp32, check=True)
+                              wl.softmax_scale, o_fp32=o_fp32, check=True, fused=fused)
     torch.cuda.synchronize()
     return o.float().cpu().numpy(), lse.cpu().numpy()
 
 
-def _check_vs_oracle(ra, wl):
+def _check_vs_oracle(ra, wl, fused=False):
     q, k, v, _ = draw_qkvdo(wl)
     o_ref, lse_ref = A.attention_fwd(q, k, v, wl.cu_seqlens, wl.causal, wl.softmax_scale)
     for fp32 in (True, False):
-        o, lse = _run_fwd(ra, wl, q, k, v, o_fp32=fp32)
+        o, lse = _run_fwd(ra, wl, q, k, v, o_fp32=fp32, fused=fused)
         assert np.isfinite(o).all() and np.isfinite(lse).all()
         bound = O_TOL if fp32 else O_TOL + np.abs(o_ref) * 2.0 ** -9
         assert (np.abs(o - o_ref) - bound).max() <= 0, (wl.name, fp32, np.abs(o - o_ref).max())
@@ -103,4 +103,47 @@ def test_llama_32k_sampled_rows(ra):
         rows = sorted(set(rng.integers(0, wl.T, 48).tolist()) | {0, 1, 2047, 2048, wl.T - 1})
         ro, rl = A.attention_rows(q, k, v, wl.cu_seqlens, rows, h, True, wl.softmax_scale)
         assert np.abs(o[rows, h] - ro).max() <= O_TOL
+        assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL
+
+
+# ---- the whole ring in one launch (ra_fwd_fused)
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_fused_multi_tile_ragged_gqa(ra, layout, causal):
+    wl = custom([1500], 4, 2, 128, 3, layout, causal, seed=11, name="ragged_gqa")
+    _check_vs_oracle(ra, wl, fused=True)
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_fused_varlen_docs_per_doc_cp(ra, d):
+    wl = custom([300, 1, 5, 777, 129, 64], 4, 1, d, [3, 1, 2, 5, 8, 1], "zigzag", True, seed=12, name="varlen")
+    _check_vs_oracle(ra, wl, fused=True)
+
+
+def test_fused_tiny_matches_oracle(ra):
+    _check_vs_oracle(ra, workload("tiny"), fused=True)
+
+
+def test_fused_equals_ring_steps_fp32(ra):
+    """One launch over the ring and one launch per ring step agree within 1e-3 (fp32 outputs)."""
+    wl = custom([2048, 700], 8, 2, 128, 4, "zigzag", True, seed=13, name="fused_vs_steps")
+    q, k, v, _ = draw_qkvdo(wl)
+    for layout in ("zigzag", "contiguous"):
+        for cp in ([4, 4], [8, 3]):
+            o1, l1 = _run_fwd(ra, wl, q, k, v, o_fp32=True, cp=cp, layout=layout)
+            o2, l2 = _run_fwd(ra, wl, q, k, v, o_fp32=True, cp=cp, layout=layout, fused=True)
+            assert np.abs(o1 - o2).max() <= RING_TOL, (layout, cp, np.abs(o1 - o2).max())
+            assert np.abs(l1 - l2).max() <= RING_TOL
+
+
+def test_fused_llama_32k_sampled_rows(ra):
+    wl = workload("llama3_8b_32k")
+    q, k, v, _ = draw_qkvdo(wl)
+    o, lse = _run_fwd(ra, wl, q, k, v, o_fp32=False, fused=True)
+    rng = np.random.default_rng(1)
+    for h in (0, 7, 30):
+        rows = sorted(set(rng.integers(0, wl.T, 48).tolist()) | {0, 1, 2047, 2048, wl.T - 1})
+        ro, rl = A.attention_rows(q, k, v, wl.cu_seqlens, rows, h, True, wl.softmax_scale)
+        assert (np.abs(o[rows, h] - ro) - (O_TOL + np.abs(ro) * 2.0 ** -9)).max() <= 0
         assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL

@@ -190,3 +190,49 @@ def test_fwd_rejects_bad_pointers_before_touching_the_gpu(ra):
     st = lib.ra_bwd(plan.handle, p(16), p(32), p(48), p(64), 0, p(80), p(96), p(112), p(128), p(144), 0,
                     p(160), 16, p(0))
     assert st == 4
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("lengths,cp", [([512], 4), ([700, 3, 1, 260], [4, 2, 1, 3]), ([130, 9], 8), ([1000], 1)])
+def test_fused_forward_tiles_cover_each_visible_pair_once(ra, layout, causal, lengths, cp):
+    """The single-launch forward visits, per query chunk, every visible key once,
+    shard by shard in ring order, and its active-tile counts match the mask."""
+    wl = custom(lengths, 2, 2, 64, cp, layout, causal)
+    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), layout, causal, 2, 2, 64)
+    items, tiles = plan.fused_items()
+    want = set()
+    for pairs in _expected(wl, causal).values():
+        want |= pairs
+    got = []
+    rows = set()
+    for q0, q1, t0, nt, na0, na1, flags, work in items:
+        assert 0 < q1 - q0 <= 256 and nt == work and flags == 1
+        rows.update(range(q0, q1))
+        last = [min(q0 + 128, q1) - 1, q1 - 1]
+        seen = [0, 0]
+        for kst, kend in tiles[t0:t0 + nt]:
+            assert kst < kend and kend - kst > 0
+            for qt in range(2):
+                if q0 + 128 * qt < q1 and (not causal or kst <= last[qt]):
+                    seen[qt] += 1
+            for q in range(q0, q1):
+                for k in range(kst, min(kst + 128, kend)):
+                    if not causal or k <= q:
+                        got.append((q, k))
+        assert seen == [na0, na1]
+        # ring order: the shards the chunk meets come as (r - s) mod cp, s = 0, 1, ...
+        d = max(i for i in range(wl.num_docs) if wl.cu_seqlens[i] <= q0)
+        base, L, c = wl.cu_seqlens[d], wl.doc_lengths[d], wl.cp_per_doc[d]
+        r = next(r for r in range(c) for a, b in R.shard_ranges(L, c, layout, r) if a <= q0 - base < b)
+        order = []
+        for kst, _ in tiles[t0:t0 + nt]:
+            j = next(j for j in range(c) for a, b in R.shard_ranges(L, c, layout, j) if a <= kst - base < b)
+            if not order or order[-1] != j:
+                order.append(j)
+        steps = [(r - j) % c for j in order]
+        assert steps == sorted(steps) and len(set(steps)) == len(steps)
+    assert len(got) == len(set(got))
+    assert set(got) == want
+    assert rows == set(range(wl.T))
+    assert plan.fused_workspace_bytes() >= 256 + 32 * len(items) + 8 * len(tiles)
