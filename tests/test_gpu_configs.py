@@ -156,3 +156,12 @@ def test_fused_forward_at_128k(ra):
         ro, rl = A.attention_rows(qs, ks, vs, wl.cu_seqlens, rows, 0, True, wl.softmax_scale)
         assert (np.abs(o[rows, h] - ro) - (O_TOL + np.abs(ro) * 2.0 ** -9)).max() <= 0
         assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL
+
+
+def test_noncausal_128k(ra):
+    """The no-mask mode at full size (every key visible to every query)."""
+    _check(ra, workload("long_128k_noncausal"), heads=(0, 21), nrows=12)
+
+
+def test_head_dim_64_at_128k(ra):
+    _check(ra, workload("long_128k_d64"), heads=(2, 30), nrows=12)
