@@ -12,7 +12,10 @@ paralelo por rango"):
 * CP group sizes are powers of two from 1 to the number of ranks;
 * a static CP size is set by the longest sequence of the batch (so shorter
   sequences are split too); the dynamic choice gives each sequence the
-  smallest group that fits the per-rank memory limit;
+  smallest group that fits the per-rank memory limit and does not leave any
+  one rank of the group more than the balanced share of the batch's time
+  (sum of time(L) over the ranks): the page wants both the compute balance
+  across data-parallel groups and no needless CP communication;
 * the page's solver is "a heuristic" without further detail.  Reading taken:
   longest-processing-time-first placement of each sequence on an aligned
   group of its size (ranks [g * cp, (g + 1) * cp)), choosing the group whose
@@ -62,10 +65,15 @@ def place(lengths, num_ranks, max_tokens_per_rank, causal=True, sec_per_pair=1.0
     base = [min_pow2_cp(L, max_tokens_per_rank, num_ranks) if L > 0 else 1 for L in lengths]
     if any(c == 0 for c in base):
         raise ValueError("a sequence exceeds the memory of all ranks")
+    times = [seq_time(L, causal, sec_per_pair, sec_per_token) for L in lengths]
     if mode == "static":
         top = max(base) if base else 1
         base = [top] * n
-    times = [seq_time(L, causal, sec_per_pair, sec_per_token) for L in lengths]
+    else:
+        share = sum(times) / num_ranks  # balanced time per rank
+        for i in range(n):
+            while base[i] < num_ranks and times[i] / base[i] > share:
+                base[i] *= 2
     order = sorted(range(n), key=lambda i: (-times[i], i))
     load = [0.0] * num_ranks
     tokens = [0] * num_ranks
