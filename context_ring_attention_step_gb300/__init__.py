@@ -9,6 +9,7 @@ from .ring_attn import (  # noqa: F401
     LAYOUTS,
     Plan,
     RingAttnError,
+    dynamic_cp,
     load_library,
     ring_attn_bwd,
     ring_attn_fwd,

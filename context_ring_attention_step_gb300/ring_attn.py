@@ -77,6 +77,9 @@ def load_library(path: str | None = None):
     lib.ra_plan_fused_workspace_bytes.restype = i32
     lib.ra_plan_fused_items.argtypes = [P, c.POINTER(i32), i64, c.POINTER(i32), i64, c.POINTER(i64), c.POINTER(i64)]
     lib.ra_plan_fused_items.restype = i32
+    lib.ra_dynamic_cp.argtypes = [c.POINTER(i32), i32, i32, i64, i32, c.c_double, c.c_double, i32,
+                                  c.POINTER(i32), c.POINTER(i32), c.POINTER(c.c_double), c.POINTER(i64)]
+    lib.ra_dynamic_cp.restype = i32
     lib.ra_workspace_status.argtypes = [P, P]
     lib.ra_workspace_status.restype = i32
     _lib = lib
@@ -260,3 +263,24 @@ def workspace_status(workspace, device=None):
     """Synchronise and return the status word of the last call on this workspace."""
     dev = workspace.device if device is None else device
     return _lib.ra_workspace_status(_ptr(workspace), _stream(dev))
+
+
+def dynamic_cp(doc_lengths, num_ranks, max_tokens_per_rank, causal=True, sec_per_pair=1.0, sec_per_token=0.0,
+               mode="dynamic"):
+    """Dynamic-CP sizing (ra_dynamic_cp): per-sequence group sizes and placement.
+
+    Returns a dict with ``cp_per_doc``, ``first_rank``, ``rank_load`` (modelled
+    seconds) and ``rank_tokens``.
+    """
+    lib = load_library()
+    n = len(doc_lengths)
+    lens = _i32_array(doc_lengths)
+    cp = (ctypes.c_int32 * max(1, n))()
+    first = (ctypes.c_int32 * max(1, n))()
+    load = (ctypes.c_double * num_ranks)()
+    tok = (ctypes.c_int64 * num_ranks)()
+    m = {"dynamic": 0, "static": 1}[mode]
+    _check(lib.ra_dynamic_cp(lens, n, int(num_ranks), int(max_tokens_per_rank), int(bool(causal)),
+                             float(sec_per_pair), float(sec_per_token), m, cp, first, load, tok))
+    return {"cp_per_doc": list(cp[:n]), "first_rank": list(first[:n]), "rank_load": list(load),
+            "rank_tokens": list(tok)}

@@ -75,6 +75,7 @@ typedef enum {
 } ra_status;
 
 typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
+typedef enum { RA_CP_DYNAMIC = 0, RA_CP_STATIC = 1 } ra_cp_mode;
 
 typedef struct ra_plan ra_plan; /* opaque, host memory only */
 
@@ -141,6 +142,33 @@ ra_status ra_plan_work_items(const ra_plan* plan, int32_t which, int32_t* items,
  */
 ra_status ra_shard_token_ranges(const ra_plan* plan, int32_t doc, int32_t rank,
                                 int32_t* begin2, int32_t* end2, int32_t* count);
+
+/*
+ * Dynamic-CP sizing (host only; Dynamic-CP page, "Modelado del programador de
+ * datos", "Necesidad de un enfoque dinamico", "Construccion de multiples
+ * grupos de contexto paralelo por rango"): a context-parallel group size per
+ * sequence and its place on num_ranks ranks, from the cost model
+ *   time(L) = sec_per_pair * pairs(L) + sec_per_token * L,
+ *   pairs(L) = L (L + 1) / 2 causal, L * L otherwise,
+ * group sizes powers of two in [1, num_ranks] (num_ranks a power of two) and
+ * at most max_tokens_per_rank tokens on a rank (a sequence of length L on a
+ * group of size c puts ceil(L / c) tokens on each of its ranks).
+ *   mode RA_CP_DYNAMIC: each sequence starts at the smallest size that fits
+ *     the token limit and keeps its per-rank time <= sum(time) / num_ranks;
+ *   mode RA_CP_STATIC: every sequence takes the size of the longest one.
+ * Sequences are placed most expensive first on the aligned group
+ * [g c, (g + 1) c) whose busiest rank ends least loaded (ties: lowest g),
+ * within the token limit; one that fits no group moves to the next larger
+ * size.  Outputs (host): cp_per_doc[num_docs] (usable as ra_plan_create's
+ * cp_size_per_doc), first_rank[num_docs], and optionally rank_load[num_ranks]
+ * (modelled seconds: sum of time(L)/c over the sequences a rank holds) and
+ * rank_tokens[num_ranks].  RA_ERR_INVALID_ARG (with a message) for bad
+ * arguments or a batch that does not fit.  No device work.
+ */
+ra_status ra_dynamic_cp(const int32_t* doc_lengths, int32_t num_docs, int32_t num_ranks,
+                        int64_t max_tokens_per_rank, int32_t causal, double sec_per_pair, double sec_per_token,
+                        int32_t mode, int32_t* cp_per_doc, int32_t* first_rank, double* rank_load,
+                        int64_t* rank_tokens);
 
 /*
  * Forward in one launch over the whole ring (same result as ra_fwd).  Each

@@ -165,3 +165,14 @@ def test_noncausal_128k(ra):
 
 def test_head_dim_64_at_128k(ra):
     _check(ra, workload("long_128k_d64"), heads=(2, 30), nrows=12)
+
+
+def test_varlen_65k_with_dynamic_cp_sizes(ra):
+    """The varlen batch with per-document cp chosen by ra_dynamic_cp (8 ranks,
+    12288 tokens per rank): same parity bar on sampled rows and identities."""
+    from workloads import custom
+    base = workload("varlen_65k")
+    lengths = base.doc_lengths
+    sizes = ra.dynamic_cp(lengths, 8, 12288)["cp_per_doc"]
+    wl = custom(lengths, base.Hq, base.Hkv, base.d, sizes, "zigzag", True, seed=base.seed, name="varlen_dynamic_cp")
+    _check(ra, wl, heads=(1, 26), nrows=24)
