@@ -86,6 +86,9 @@ __global__ void __launch_bounds__(384, 1)
 
   // A CTA of this grid already gave up: do no work (fail fast, no waits).
   if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
+  // Ring-step launches: the next step may start on the SMs this grid frees;
+  // it reads the running (O, LSE) only after this grid has completed.
+  if constexpr (!kFused) pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int h = blockIdx.x % p.Hq;
   const int g = h / (p.Hq / p.Hkv);
@@ -454,6 +457,7 @@ __global__ void __launch_bounds__(384, 1)
           }
         }
       } else if (ok) {
+        pdl_wait();  // the previous ring step's (O, LSE) are complete and visible
         const bool valid = row < it.q1;
         const bool first = (it.flags & kFirstStep) != 0;
         const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
@@ -510,6 +514,8 @@ __global__ void __launch_bounds__(384, 1)
     }
   }
 
+  // keep the launches' completion order: this grid completes after the previous one
+  if (!kFused && threadIdx.x == 0 && blockIdx.x == gridDim.x - 1) pdl_wait();
   __syncwarp();
   tc_fence_before();
   __syncthreads();
@@ -527,8 +533,17 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items * p.Hq;
   if (grid <= 0) return cudaSuccess;
-  kern<<<(unsigned)grid, 384, FwdCfg<D>::kSmem, stream>>>(tq, tk, tv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3((unsigned)grid);
+  cfg.blockDim = dim3(384);
+  cfg.dynamicSmemBytes = FwdCfg<D>::kSmem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = kFused ? 0 : 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
 }
 
 }  // namespace

@@ -73,6 +73,14 @@ __device__ __forceinline__ void add_bf16x2_to(float& acc_lo, float& acc_hi, uint
       : "r"(pk));
 }
 
+// Programmatic dependent launch (ring-step launches on one stream): let the
+// next launch's CTAs start on SMs this grid frees, and wait for the previous
+// grid's completion (and memory) only where its results are used.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
