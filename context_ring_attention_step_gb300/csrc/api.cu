@@ -53,6 +53,7 @@ ra_status fail(ra_status st, const char* fmt, ...) {
 }
 
 constexpr size_t kHeader = 256;
+constexpr int kSelfTestSite = 900;  // status code of the failure-detection self-test
 constexpr size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Chunk boundaries of one document of length L (document-local):
@@ -735,6 +736,17 @@ ra_status ra_bwd(const ra_plan* P, const void* q, const void* k, const void* v, 
     rs = ra_bwd_ring_step(P, s, q, k, v, dout, dq, dk, dv, grads_fp32, workspace, workspace_bytes, stream);
   if (rs == RA_OK) rs = ra_bwd_finish(P, dq, dk, dv, grads_fp32, workspace, workspace_bytes, stream);
   return rs;
+}
+
+ra_status ra_selftest_wait_timeout(void* workspace, uint32_t limit_us, void* stream_) {
+  if (!workspace || !aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace must be a 16-byte aligned device pointer");
+  if (limit_us < 1 || limit_us > 4000000) return fail(RA_ERR_INVALID_ARG, "limit_us must be in [1, 4000000]");
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = cudaMemsetAsync(workspace, 0, kHeader, st);
+  if (e == cudaSuccess) e = ra::launch_wait_timeout_probe(reinterpret_cast<int*>(workspace), (uint64_t)limit_us * 1000u,
+                                                          kSelfTestSite, st);
+  if (e != cudaSuccess) return cuda_fail(e, "self-test launch");
+  return RA_OK;
 }
 
 ra_status ra_workspace_status(const void* workspace, void* stream_) {

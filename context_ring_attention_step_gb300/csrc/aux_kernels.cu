@@ -5,9 +5,29 @@
 #include <cuda_bf16.h>
 
 #include "ring_attn_internal.h"
+#include "tc.cuh"
 
 namespace ra {
 namespace {
+
+// Failure-detection self-test: one thread waits, with a short limit, on an
+// mbarrier that nothing ever arrives on, through the same bounded wait the
+// ring kernels use; it gives up, records `site` in the status word and the
+// kernel returns.
+__global__ void wait_timeout_probe_kernel(int* status, uint64_t limit_ns, int site) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    const Abort ab{&abort_flag, status};
+    (void)mbar_wait(smem_u32(&bar), 0, ab, site, limit_ns);
+  }
+}
 
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -103,6 +123,11 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout
     bwd_preprocess_kernel<64><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
   else
     return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, int site, cudaStream_t stream) {
+  wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(status, limit_ns, site);
   return cudaGetLastError();
 }
 

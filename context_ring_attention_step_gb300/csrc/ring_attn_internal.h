@@ -82,6 +82,7 @@ cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorM
                             int num_items, cudaStream_t stream);
 // o (bf16) = o_run (fp32), elementwise.
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
+cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, int site, cudaStream_t stream);
 // Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e);
 // both written with row pitch `pitch` (>= T).
 cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout, const float* lse,

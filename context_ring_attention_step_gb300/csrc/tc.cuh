@@ -123,7 +123,8 @@ struct Abort {
   int* status;         // global status word (workspace header)
 };
 
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab, int site) {
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const Abort& ab, int site,
+                                          uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t n = 0;
@@ -131,7 +132,7 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, const A
     if (mbar_try_wait(bar, parity)) return true;
     if ((++n & 63u) == 0) {
       if (*ab.flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      if (globaltimer_ns() - t0 > limit_ns) {
         *ab.flag = 1;
         atomicCAS(ab.status, 0, site);
         return false;

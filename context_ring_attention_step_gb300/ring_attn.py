@@ -80,6 +80,8 @@ def load_library(path: str | None = None):
     lib.ra_dynamic_cp.argtypes = [c.POINTER(i32), i32, i32, i64, i32, c.c_double, c.c_double, i32,
                                   c.POINTER(i32), c.POINTER(i32), c.POINTER(c.c_double), c.POINTER(i64)]
     lib.ra_dynamic_cp.restype = i32
+    lib.ra_selftest_wait_timeout.argtypes = [P, c.c_uint32, P]
+    lib.ra_selftest_wait_timeout.restype = i32
     lib.ra_workspace_status.argtypes = [P, P]
     lib.ra_workspace_status.restype = i32
     _lib = lib

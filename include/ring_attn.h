@@ -271,6 +271,17 @@ ra_status ra_bwd_finish(const ra_plan* plan, void* dq, void* dk, void* dv, int32
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * Failure-detection self-test (no counterpart on the pages): enqueue one small
+ * kernel that waits, through the same bounded mbarrier wait the ring kernels
+ * use, on a barrier that nothing ever arrives on.  After limit_us microseconds
+ * (1 .. 4000000) it gives up, writes site code 900 into the status word at the
+ * start of `workspace` (device, >= 256 bytes, zeroed here first) and returns,
+ * so ra_workspace_status() then reports RA_ERR_TIMEOUT and the CUDA context
+ * stays usable.  No trap, no hang.  RA_ERR_INVALID_ARG for bad arguments.
+ */
+ra_status ra_selftest_wait_timeout(void* workspace, uint32_t limit_us, void* stream);
+
+/*
  * Synchronise `stream` and read the status word that the last ra_fwd/ra_bwd
  * call on this workspace left in its header: RA_OK, or RA_ERR_TIMEOUT if a
  * kernel gave up on a pipeline wait (its outputs are then undefined).
