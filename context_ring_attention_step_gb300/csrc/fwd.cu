@@ -282,6 +282,13 @@ __global__ void __launch_bounds__(384, 1)
     int u = 0;  // tiles done so far
     for (int j = 0; j < tl.n; ++j) {
       if (!active(j, qa, my_last, na)) continue;
+      if (!kFused && u == na - 1 && row < it.q1 && !(it.flags & kFirstStep)) {
+        // last tile: bring this row's running (O, LSE) towards L2 for the merge
+        const char* orow = reinterpret_cast<const char*>(p.o_run + ((size_t)row * p.Hq + h) * D);
+#pragma unroll
+        for (int c = 0; c < D * 4; c += 128) prefetch_l2(orow + c);
+        prefetch_l2(p.lse + (size_t)h * p.T + row);
+      }
       if (!mbar_wait(b_s + 8 * qt, sph, ab, 110)) { ok = false; break; }
       sph ^= 1;
       tc_fence_after();
@@ -464,7 +471,19 @@ __global__ void __launch_bounds__(384, 1)
         const float inv_l = (l_rnd > 0.f) ? 1.f / l_rnd : 0.f;
         float* lse_ptr = p.lse + (size_t)h * p.T + row;
         float* orow = p.o_run + ((size_t)row * p.Hq + h) * D;
+        // Issue the loads of the previous running state together (the LSE and
+        // the whole fp32 row): one memory round trip, not one per chunk.
+        const bool may_read = valid && !first && lse_b != kNegInf;
         const float lse_a = (valid && !first) ? *lse_ptr : kNegInf;
+        float4 old[D / 4];
+        if (may_read) {
+          const float4* src = reinterpret_cast<const float4*>(orow);
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) old[i] = src[i];
+        } else {
+#pragma unroll
+          for (int i = 0; i < D / 4; ++i) old[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         float wa = 0.f, wb = 1.f, lse_new = lse_b;
         if (lse_b == kNegInf) { wa = 1.f; wb = 0.f; lse_new = lse_a; }
         else if (lse_a != kNegInf) {
@@ -477,7 +496,7 @@ __global__ void __launch_bounds__(384, 1)
         }
         wb *= inv_l;
         const bool write = valid && (first || lse_b != kNegInf);
-        const bool read_old = valid && !first && lse_a != kNegInf && lse_b != kNegInf;
+        const bool read_old = may_read && lse_a != kNegInf;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -499,7 +518,7 @@ __global__ void __launch_bounds__(384, 1)
               v.z = __uint_as_float(o[4 * i + 2]) * wb;
               v.w = __uint_as_float(o[4 * i + 3]) * wb;
               if (read_old) {
-                const float4 u = dst[i];
+                const float4 u = old[8 * c + i];
                 v.x = fmaf(wa, u.x, v.x);
                 v.y = fmaf(wa, u.y, v.y);
                 v.z = fmaf(wa, u.z, v.z);
