@@ -426,8 +426,9 @@ def main():
 
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs from pinned host memory and its results back
-    # (o, lse, dq, dk, dv), through the public Python API.  The copies run on a
-    # second stream, double-buffered: step i+1's inputs go up while step i
+    # (o, lse, dq, dk, dv), through the public Python API.  Uploads and
+    # downloads run on two streams of their own (both directions of the host
+    # link at once), double-buffered: step i+1's inputs go up while step i
     # computes, and step i's results come down while step i+1 computes.  The
     # timed region runs from the first copy to the end of the last one.
     e2e = None
@@ -441,7 +442,7 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in pin)
         d2h = sum(x.numel() * x.element_size() for x in outs_h[0])
         ins = [[torch.empty_like(x, device=dev) for x in pin] for _ in range(2)]
-        cstream = torch.cuda.Stream(dev)
+        up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)  # both link directions at once
         ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of a buffer landed
         ev_used = [torch.cuda.Event() for _ in range(2)]   # compute done with a buffer
         ev_out = torch.cuda.Event()
@@ -450,16 +451,17 @@ def main():
             dist.barrier()
         a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a0.record(stream)
-        cstream.wait_stream(stream)
+        up_stream.wait_stream(stream)
+        down_stream.wait_stream(stream)
 
         def upload(i):
             b = i % 2
-            with torch.cuda.stream(cstream):
+            with torch.cuda.stream(up_stream):
                 if i >= 2:
-                    cstream.wait_event(ev_used[b])
+                    up_stream.wait_event(ev_used[b])
                 for dst, src in zip(ins[b], pin):
                     dst.copy_(src, non_blocking=True)
-                ev_in[b].record(cstream)
+                ev_in[b].record(up_stream)
 
         upload(0)
         for i in range(args.e2e_steps):
@@ -474,19 +476,20 @@ def main():
                                           wl.softmax_scale, plan=plan, workspace=ws_b)
             ev_used[b].record(stream)
             ev_out.record(stream)
-            with torch.cuda.stream(cstream):
-                cstream.wait_event(ev_out)
+            with torch.cuda.stream(down_stream):
+                down_stream.wait_event(ev_out)
                 for dst, src in zip(outs_h[b], (oo, ll, gq, gk, gv)):
-                    src.record_stream(cstream)
+                    src.record_stream(down_stream)
                     dst.copy_(src, non_blocking=True)
-        stream.wait_stream(cstream)
+        stream.wait_stream(up_stream)
+        stream.wait_stream(down_stream)
         a1.record(stream)
         torch.cuda.synchronize()
         e_ms = max_over_ranks(a0.elapsed_time(a1), dist, dev)
         e2e = {"value": whole_job_tflops(world, ff + fb, args.e2e_steps, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e_ms / args.e2e_steps,
-               "copies": "pinned host <-> device on a second stream, double-buffered, overlapping compute"}
+               "copies": "pinned host <-> device, uploads and downloads on two streams, double-buffered, overlapping compute"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
