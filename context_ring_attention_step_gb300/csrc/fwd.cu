@@ -420,48 +420,72 @@ __global__ void __launch_bounds__(384, 1)
       l_rnd += (lr0 + lr1) + (lr2 + lr3);
       ++u;
     }
+    // the epilogue exchanges values between lanes: the whole warp takes it or
+    // skips it (a wait that gave up in any lane has already raised the abort)
+    ok = __all_sync(0xffffffffu, ok);
     if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
       if (na > 0) {
         ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
         tc_fence_after();
       }
+      ok = __all_sync(0xffffffffu, ok);
       if (ok && kFused) {
         // the whole ring is done: O = (sum of P V) / (sum of the bf16 P), final LSE
         const bool valid = row < it.q1;
         const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
         const float inv_l = (l_rnd > 0.f) ? 1.f / l_rnd : 0.f;
         if (valid) p.lse[(size_t)h * p.T + row] = lse_b;
-        const size_t obase = ((size_t)row * p.Hq + h) * D;
+        // rows leave through this warp's slice of its Q tile's buffer, so each
+        // store instruction covers whole rows (as in the ring-step merge below)
+        constexpr int kHalf = D / 2;
+        constexpr int kChunks = kHalf / 4;
+        constexpr int kPer = 32 / kChunks;
+        constexpr int kSteps = 32 / kPer;
+        const uint32_t scratch = sQ + qt * C::kTile + (uint32_t)(warp & 3) * (C::kTile / 4);
+        const int sub = lane / kChunks, ch = lane % kChunks;
+        const int wrow0 = row0 + (int)lane_base;
+        const size_t obase = ((size_t)wrow0 * p.Hq + h) * D + 4 * ch;
+        const size_t rstride = (size_t)p.Hq * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (na > 0) {
-            tmem_ld32(tO + 32 * c, o);
-            tmem_ld_wait();
-            reg_fence32(o);
-          } else {
+        for (int ps = 0; ps < 2; ++ps) {
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
-          }
-          if (!valid) continue;
-          if (p.o_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(p.o_out) + obase + 32 * c);
+          for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t o[32];
+            if (na > 0) {
+              tmem_ld32(tO + ps * kHalf + 32 * c, o);
+              tmem_ld_wait();
+              reg_fence32(o);
+            } else {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 w;
-              w.x = pack_bf16x2(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              w.y = pack_bf16x2(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              w.z = pack_bf16x2(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              w.w = pack_bf16x2(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[i] = w;
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
             }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o_out) + obase + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
-              dst[i] = make_float4(__uint_as_float(o[4 * i + 0]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
-                                   __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
+            for (int k = 0; k < 8; ++k) {
+              const int kc = 8 * c + k;
+              const uint32_t addr = scratch + (uint32_t)lane * (kHalf * 4) + (uint32_t)((kc ^ (lane % kChunks)) << 4);
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                           "f"(__uint_as_float(o[4 * k]) * inv_l), "f"(__uint_as_float(o[4 * k + 1]) * inv_l),
+                           "f"(__uint_as_float(o[4 * k + 2]) * inv_l), "f"(__uint_as_float(o[4 * k + 3]) * inv_l)
+                           : "memory");
+            }
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < kSteps; ++i) {
+            const int rr = kPer * i + sub;
+            float4 v;
+            const uint32_t addr = scratch + (uint32_t)rr * (kHalf * 4) + (uint32_t)((ch ^ (rr % kChunks)) << 4);
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+            if (wrow0 + rr >= it.q1) continue;
+            const size_t off = obase + rr * rstride + ps * kHalf;
+            if (p.o_bf16)
+              *reinterpret_cast<uint2*>(reinterpret_cast<uint16_t*>(p.o_out) + off) =
+                  make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
+            else
+              *reinterpret_cast<float4*>(reinterpret_cast<float*>(p.o_out) + off) = v;
+          }
+          __syncwarp();
         }
       } else if (ok) {
         pdl_wait();  // the previous ring step's (O, LSE) are complete and visible
@@ -470,20 +494,7 @@ __global__ void __launch_bounds__(384, 1)
         const float lse_b = (l_sum > 0.f) ? (m_ref + log2f(l_sum)) * kLn2 : kNegInf;
         const float inv_l = (l_rnd > 0.f) ? 1.f / l_rnd : 0.f;
         float* lse_ptr = p.lse + (size_t)h * p.T + row;
-        float* orow = p.o_run + ((size_t)row * p.Hq + h) * D;
-        // Issue the loads of the previous running state together (the LSE and
-        // the whole fp32 row): one memory round trip, not one per chunk.
-        const bool may_read = valid && !first && lse_b != kNegInf;
         const float lse_a = (valid && !first) ? *lse_ptr : kNegInf;
-        float4 old[D / 4];
-        if (may_read) {
-          const float4* src = reinterpret_cast<const float4*>(orow);
-#pragma unroll
-          for (int i = 0; i < D / 4; ++i) old[i] = src[i];
-        } else {
-#pragma unroll
-          for (int i = 0; i < D / 4; ++i) old[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-        }
         float wa = 0.f, wb = 1.f, lse_new = lse_b;
         if (lse_b == kNegInf) { wa = 1.f; wb = 0.f; lse_new = lse_a; }
         else if (lse_a != kNegInf) {
@@ -496,37 +507,75 @@ __global__ void __launch_bounds__(384, 1)
         }
         wb *= inv_l;
         const bool write = valid && (first || lse_b != kNegInf);
-        const bool read_old = may_read && lse_a != kNegInf;
+        const bool read_old = valid && !first && lse_a != kNegInf && lse_b != kNegInf;
+        // The running rows are read and written whole, through this warp's
+        // slice of its Q tile's buffer (free: the tile's last QK is done):
+        // the thread of a row writes its columns there, then every load and
+        // store instruction covers kPer full rows (16 bytes per lane), instead
+        // of 16 bytes of 32 different rows.  Two passes of D/2 columns.
+        constexpr int kHalf = D / 2;          // columns per pass
+        constexpr int kChunks = kHalf / 4;    // 16-byte chunks of a row per pass
+        constexpr int kPer = 32 / kChunks;    // rows per instruction
+        constexpr int kSteps = 32 / kPer;     // instructions per pass
+        const uint32_t scratch = sQ + qt * C::kTile + (uint32_t)(warp & 3) * (C::kTile / 4);
+        const int sub = lane / kChunks, ch = lane % kChunks;
+        const int wrow0 = row0 + (int)lane_base;  // the warp's first row
+        float* obase = p.o_run + ((size_t)wrow0 * p.Hq + h) * D + 4 * ch;
+        const size_t rstride = (size_t)p.Hq * D;
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          if (na > 0) {
-            tmem_ld32(tO + 32 * c, o);
-            tmem_ld_wait();
-            reg_fence32(o);
-          } else {
+        for (int ps = 0; ps < 2; ++ps) {
+          // this pass's loads of the old rows first (one round trip; the rows
+          // were hinted into L2 during the last key tile)
+          float4 old[kSteps];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          for (int i = 0; i < kSteps; ++i) {
+            const int rr = kPer * i + sub;
+            const bool ro = __shfl_sync(0xffffffffu, read_old, rr) != 0;
+            old[i] = ro ? *reinterpret_cast<const float4*>(obase + rr * rstride + ps * kHalf)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
           }
-          if (write) {
-            float4* dst = reinterpret_cast<float4*>(orow + 32 * c);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              float4 v;
-              v.x = __uint_as_float(o[4 * i + 0]) * wb;
-              v.y = __uint_as_float(o[4 * i + 1]) * wb;
-              v.z = __uint_as_float(o[4 * i + 2]) * wb;
-              v.w = __uint_as_float(o[4 * i + 3]) * wb;
-              if (read_old) {
-                const float4 u = old[8 * c + i];
-                v.x = fmaf(wa, u.x, v.x);
-                v.y = fmaf(wa, u.y, v.y);
-                v.z = fmaf(wa, u.z, v.z);
-                v.w = fmaf(wa, u.w, v.w);
-              }
-              dst[i] = v;
+          for (int c = 0; c < kHalf / 32; ++c) {
+            uint32_t o[32];
+            if (na > 0) {
+              tmem_ld32(tO + ps * kHalf + 32 * c, o);
+              tmem_ld_wait();
+              reg_fence32(o);
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i) o[i] = 0u;
+            }
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+              const int kc = 8 * c + k;  // chunk within the pass
+              const uint32_t addr = scratch + (uint32_t)lane * (kHalf * 4) + (uint32_t)((kc ^ (lane % kChunks)) << 4);
+              asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr),
+                           "f"(__uint_as_float(o[4 * k]) * wb), "f"(__uint_as_float(o[4 * k + 1]) * wb),
+                           "f"(__uint_as_float(o[4 * k + 2]) * wb), "f"(__uint_as_float(o[4 * k + 3]) * wb)
+                           : "memory");
             }
           }
+          __syncwarp();
+#pragma unroll
+          for (int i = 0; i < kSteps; ++i) {
+            const int rr = kPer * i + sub;
+            const float w = __shfl_sync(0xffffffffu, wa, rr);
+            const bool ro = __shfl_sync(0xffffffffu, read_old, rr) != 0;
+            const bool wr = __shfl_sync(0xffffffffu, write, rr) != 0;
+            float4 v;
+            const uint32_t addr = scratch + (uint32_t)rr * (kHalf * 4) + (uint32_t)((ch ^ (rr % kChunks)) << 4);
+            asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                         : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr) : "memory");
+            if (ro) {
+              const float4 u = old[i];
+              v.x = fmaf(w, u.x, v.x);
+              v.y = fmaf(w, u.y, v.y);
+              v.z = fmaf(w, u.z, v.z);
+              v.w = fmaf(w, u.w, v.w);
+            }
+            if (wr) *reinterpret_cast<float4*>(obase + rr * rstride + ps * kHalf) = v;
+          }
+          __syncwarp();  // the next pass reuses the slice
         }
         if (write) *lse_ptr = lse_new;
       }
