@@ -428,9 +428,11 @@ def main():
     # Every step copies its inputs from pinned host memory and its results back
     # (o, lse, dq, dk, dv), through the public Python API.  Uploads and
     # downloads run on two streams of their own (both directions of the host
-    # link at once), double-buffered: step i+1's inputs go up while step i
-    # computes, and step i's results come down while step i+1 computes.  The
-    # timed region runs from the first copy to the end of the last one.
+    # link at once), double-buffered in device inputs and outputs (passed as
+    # out=, so nothing is allocated in the timed loop): step i+1's inputs go up
+    # while step i computes, and step i's results come down while step i+1
+    # computes.  The timed region runs from the first copy to the end of the
+    # last one.
     e2e = None
     if args.e2e_steps > 0:
         pin = [x.pin_memory() for x in (q_h, k_h, v_h, do_h)]
@@ -442,6 +444,8 @@ def main():
         h2d = sum(x.numel() * x.element_size() for x in pin)
         d2h = sum(x.numel() * x.element_size() for x in outs_h[0])
         ins = [[torch.empty_like(x, device=dev) for x in pin] for _ in range(2)]
+        outs_d = [[torch.empty(x.shape, dtype=x.dtype, device=dev) for x in outs_h[0]] for _ in range(2)]
+        ev_down = [torch.cuda.Event() for _ in range(2)]   # a device output buffer has been copied out
         up_stream, down_stream = torch.cuda.Stream(dev), torch.cuda.Stream(dev)  # both link directions at once
         ev_in = [torch.cuda.Event() for _ in range(2)]     # inputs of a buffer landed
         ev_used = [torch.cuda.Event() for _ in range(2)]   # compute done with a buffer
@@ -469,18 +473,21 @@ def main():
             if i + 1 < args.e2e_steps:
                 upload(i + 1)
             stream.wait_event(ev_in[b])
+            if i >= 2:
+                stream.wait_event(ev_down[b])
             qd, kd, vd, dod = ins[b]
-            oo, ll = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale,
-                                      plan=plan, workspace=ws_f)
-            gq, gk, gv = ra.ring_attn_bwd(qd, kd, vd, oo, dod, ll, wl.cu_seqlens, cps, wl.layout, wl.causal,
-                                          wl.softmax_scale, plan=plan, workspace=ws_b)
+            oo, ll, gq, gk, gv = outs_d[b]
+            ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale,
+                             plan=plan, workspace=ws_f, out=(oo, ll))
+            ra.ring_attn_bwd(qd, kd, vd, oo, dod, ll, wl.cu_seqlens, cps, wl.layout, wl.causal,
+                             wl.softmax_scale, plan=plan, workspace=ws_b, out=(gq, gk, gv))
             ev_used[b].record(stream)
             ev_out.record(stream)
             with torch.cuda.stream(down_stream):
                 down_stream.wait_event(ev_out)
-                for dst, src in zip(outs_h[b], (oo, ll, gq, gk, gv)):
-                    src.record_stream(down_stream)
+                for dst, src in zip(outs_h[b], outs_d[b]):
                     dst.copy_(src, non_blocking=True)
+                ev_down[b].record(down_stream)
         stream.wait_stream(up_stream)
         stream.wait_stream(down_stream)
         a1.record(stream)
@@ -489,7 +496,7 @@ def main():
         e2e = {"value": whole_job_tflops(world, ff + fb, args.e2e_steps, e_ms), "unit": "TFLOP/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
                "ms_per_step": e_ms / args.e2e_steps,
-               "copies": "pinned host <-> device, uploads and downloads on two streams, double-buffered, overlapping compute"}
+               "copies": "pinned host <-> device, uploads and downloads on two streams, double-buffered device inputs and outputs (no allocation in the timed loop), overlapping compute"}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -199,12 +199,13 @@ def _check_tensor(name, t, shape, dtype):
 
 
 def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, scale=None,
-                  o_fp32=False, plan=None, workspace=None, check=False, fused=False):
+                  o_fp32=False, plan=None, workspace=None, check=False, fused=False, out=None):
     """Ring attention forward: returns (o [T,Hq,d], lse [Hq,T] fp32).
 
     ``fused=True`` runs the whole ring in one launch (ra_fwd_fused) instead of
-    one launch per ring step.  ``check=True`` synchronises and raises if a
-    kernel reported a timeout.
+    one launch per ring step.  ``out=(o, lse)`` writes into caller-owned
+    tensors instead of allocating them.  ``check=True`` synchronises and
+    raises if a kernel reported a timeout.
     """
     T, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -214,8 +215,14 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, sc
     _check_tensor("k", k, (T, Hkv, D), torch.bfloat16)
     _check_tensor("v", v, (T, Hkv, D), torch.bfloat16)
     dev = q.device
-    o = torch.empty((T, Hq, D), dtype=torch.float32 if o_fp32 else torch.bfloat16, device=dev)
-    lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    ot = torch.float32 if o_fp32 else torch.bfloat16
+    if out is None:
+        o = torch.empty((T, Hq, D), dtype=ot, device=dev)
+        lse = torch.empty((Hq, T), dtype=torch.float32, device=dev)
+    else:
+        o, lse = out
+        _check_tensor("o", o, (T, Hq, D), ot)
+        _check_tensor("lse", lse, (Hq, T), torch.float32)
     ws_bytes = plan.fused_workspace_bytes() if fused else plan.workspace_bytes(o_fp32=o_fp32)[0]
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
@@ -228,10 +235,12 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, sc
 
 
 def ring_attn_bwd(q, k, v, o, do, lse, cu_seqlens, cp_size, layout="zigzag", causal=True, scale=None,
-                  grads_fp32=False, plan=None, workspace=None, check=False):
+                  grads_fp32=False, plan=None, workspace=None, check=False, out=None):
     """Ring attention backward from the saved LSE: returns (dq, dk, dv).
 
-    ``check=True`` synchronises and raises if a kernel reported a timeout.
+    ``out=(dq, dk, dv)`` writes into caller-owned tensors instead of
+    allocating them.  ``check=True`` synchronises and raises if a kernel
+    reported a timeout.
     """
     T, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -247,9 +256,15 @@ def ring_attn_bwd(q, k, v, o, do, lse, cu_seqlens, cp_size, layout="zigzag", cau
     _check_tensor("o", o, (T, Hq, D), o.dtype)
     dev = q.device
     gt = torch.float32 if grads_fp32 else torch.bfloat16
-    dq = torch.empty((T, Hq, D), dtype=gt, device=dev)
-    dk = torch.empty((T, Hkv, D), dtype=gt, device=dev)
-    dv = torch.empty((T, Hkv, D), dtype=gt, device=dev)
+    if out is None:
+        dq = torch.empty((T, Hq, D), dtype=gt, device=dev)
+        dk = torch.empty((T, Hkv, D), dtype=gt, device=dev)
+        dv = torch.empty((T, Hkv, D), dtype=gt, device=dev)
+    else:
+        dq, dk, dv = out
+        _check_tensor("dq", dq, (T, Hq, D), gt)
+        _check_tensor("dk", dk, (T, Hkv, D), gt)
+        _check_tensor("dv", dv, (T, Hkv, D), gt)
     ws_bytes = plan.workspace_bytes(grads_fp32=grads_fp32)[1]
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)

@@ -147,3 +147,28 @@ def test_fused_llama_32k_sampled_rows(ra):
         ro, rl = A.attention_rows(q, k, v, wl.cu_seqlens, rows, h, True, wl.softmax_scale)
         assert (np.abs(o[rows, h] - ro) - (O_TOL + np.abs(ro) * 2.0 ** -9)).max() <= 0
         assert np.abs(lse[h, rows] - rl).max() <= LSE_TOL
+
+
+def test_caller_owned_outputs(ra):
+    """out= writes the same values into caller tensors (forward and backward),
+    and a mis-shaped or mis-typed output is refused before any launch."""
+    wl = custom([700, 300], 4, 2, 128, 2, "zigzag", True, seed=31, name="out_param")
+    q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
+    cps = list(wl.cp_per_doc)
+    args = (wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale)
+    o_ref, lse_ref = ra.ring_attn_fwd(q, k, v, *args)
+    o = torch.full_like(o_ref, float("nan"))
+    lse = torch.full_like(lse_ref, float("nan"))
+    r = ra.ring_attn_fwd(q, k, v, *args, out=(o, lse))
+    assert r[0] is o and r[1] is lse
+    g_ref = ra.ring_attn_bwd(q, k, v, o_ref, do, lse_ref, *args)
+    g = tuple(torch.full_like(x, float("nan")) for x in g_ref)
+    r = ra.ring_attn_bwd(q, k, v, o, do, lse, *args, out=g)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_ref) and torch.equal(lse, lse_ref)  # the forward has no atomics
+    for a, b in zip(g, g_ref):  # dQ is summed with atomic adds: equal up to bf16 rounding
+        assert torch.allclose(a.float(), b.float(), rtol=2 ** -7, atol=1e-5)
+    with pytest.raises(ValueError):
+        ra.ring_attn_fwd(q, k, v, *args, out=(o.float(), lse))
+    with pytest.raises(ValueError):
+        ra.ring_attn_bwd(q, k, v, o, do, lse, *args, out=(g[0], g[1], g[2][:-1]))
