@@ -268,7 +268,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_128k")
-    ap.add_argument("--e2e-steps", type=int, default=4)
+    ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-tokens", type=int, default=12288)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
