@@ -8,10 +8,12 @@ thin Python binding.
 from .ring_attn import (  # noqa: F401
     LAYOUTS,
     Plan,
+    RingAttention,
     RingAttnError,
     dynamic_cp,
     load_library,
     ring_attn_bwd,
     ring_attn_fwd,
+    ring_attention,
     workspace_status,
 )

@@ -276,6 +276,36 @@ def ring_attn_bwd(q, k, v, o, do, lse, cu_seqlens, cp_size, layout="zigzag", cau
     return dq, dk, dv
 
 
+class RingAttention(torch.autograd.Function):
+    """Autograd wrapper: the forward runs ring_attn_fwd and saves (q, k, v, o,
+    lse); the backward runs ring_attn_bwd from the saved LSE.  Gradients flow
+    to q, k and v only.  Use ``ring_attention(...)``."""
+
+    @staticmethod
+    def forward(ctx, q, k, v, cu_seqlens, cp_size, layout, causal, scale, plan):
+        o, lse = ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout, causal, scale, plan=plan)
+        ctx.save_for_backward(q, k, v, o, lse)
+        ctx.args = (cu_seqlens, cp_size, layout, causal, scale, plan)
+        ctx.mark_non_differentiable(lse)
+        return o, lse
+
+    @staticmethod
+    def backward(ctx, do, _dlse):
+        q, k, v, o, lse = ctx.saved_tensors
+        cu_seqlens, cp_size, layout, causal, scale, plan = ctx.args
+        dq, dk, dv = ring_attn_bwd(q, k, v, o, do.contiguous().to(torch.bfloat16), lse, cu_seqlens, cp_size,
+                                   layout, causal, scale, plan=plan)
+        return dq, dk, dv, None, None, None, None, None, None
+
+
+def ring_attention(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, scale=None, plan=None):
+    """Differentiable ring attention: returns (o, lse); o.backward(dO) fills
+    q.grad, k.grad and v.grad through the ring backward."""
+    if plan is None:
+        plan = Plan(cu_seqlens, cp_size, layout, causal, q.shape[1], k.shape[1], q.shape[2], scale)
+    return RingAttention.apply(q, k, v, cu_seqlens, cp_size, layout, causal, scale, plan)
+
+
 def workspace_status(workspace, device=None):
     """Synchronise and return the status word of the last call on this workspace."""
     dev = workspace.device if device is None else device

@@ -172,3 +172,22 @@ def test_caller_owned_outputs(ra):
         ra.ring_attn_fwd(q, k, v, *args, out=(o.float(), lse))
     with pytest.raises(ValueError):
         ra.ring_attn_bwd(q, k, v, o, do, lse, *args, out=(g[0], g[1], g[2][:-1]))
+
+
+def test_autograd_wrapper_matches_explicit_calls(ra):
+    """ring_attention under autograd gives the forward's (o, lse) and, from
+    o.backward(dO), the explicit backward's dq, dk, dv."""
+    wl = custom([640, 200], 4, 2, 128, 2, "zigzag", True, seed=33, name="autograd")
+    q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
+    cps = list(wl.cp_per_doc)
+    args = (wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale)
+    o_ref, lse_ref = ra.ring_attn_fwd(q, k, v, *args)
+    g_ref = ra.ring_attn_bwd(q, k, v, o_ref, do, lse_ref, *args)
+    qa, ka, va = (x.clone().requires_grad_(True) for x in (q, k, v))
+    o, lse = ra.ring_attention(qa, ka, va, *args)
+    o.backward(do)
+    torch.cuda.synchronize()
+    assert torch.equal(o.detach(), o_ref) and torch.equal(lse, lse_ref)
+    for a, b in zip((qa.grad, ka.grad, va.grad), g_ref):
+        assert a.dtype == b.dtype and a.shape == b.shape
+        assert torch.allclose(a.float(), b.float(), rtol=2 ** -7, atol=1e-5)
