@@ -424,11 +424,13 @@ __global__ void __launch_bounds__(384, 1)
     // skips it (a wait that gave up in any lane has already raised the abort)
     ok = __all_sync(0xffffffffu, ok);
     if (ok && qa && (na > 0 || (it.flags & kFirstStep))) {
-      if (na > 0) {
-        ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
-        tc_fence_after();
+      if constexpr (kFused) {
+        if (na > 0) {
+          ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
+          tc_fence_after();
+        }
+        ok = __all_sync(0xffffffffu, ok);
       }
-      ok = __all_sync(0xffffffffu, ok);
       if (ok && kFused) {
         // the whole ring is done: O = (sum of P V) / (sum of the bf16 P), final LSE
         const bool valid = row < it.q1;
@@ -522,11 +524,12 @@ __global__ void __launch_bounds__(384, 1)
         const int wrow0 = row0 + (int)lane_base;  // the warp's first row
         float* obase = p.o_run + ((size_t)wrow0 * p.Hq + h) * D + 4 * ch;
         const size_t rstride = (size_t)p.Hq * D;
-#pragma unroll
-        for (int ps = 0; ps < 2; ++ps) {
-          // this pass's loads of the old rows first (one round trip; the rows
-          // were hinted into L2 during the last key tile)
-          float4 old[kSteps];
+        // A pass's loads of the old rows go out together (one round trip; the
+        // rows were hinted into L2 during the last key tile).  The first
+        // pass's go out before the wait for the final O: they need only the
+        // previous ring step.
+        float4 old[kSteps];
+        auto load_old = [&](int ps) {
 #pragma unroll
           for (int i = 0; i < kSteps; ++i) {
             const int rr = kPer * i + sub;
@@ -534,6 +537,16 @@ __global__ void __launch_bounds__(384, 1)
             old[i] = ro ? *reinterpret_cast<const float4*>(obase + rr * rstride + ps * kHalf)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
           }
+        };
+        load_old(0);
+        if (na > 0) {
+          ok = mbar_wait(b_s + 8 * qt, sph, ab, 111);  // O final
+          tc_fence_after();
+        }
+        ok = __all_sync(0xffffffffu, ok);
+#pragma unroll
+        for (int ps = 0; ps < 2 && ok; ++ps) {
+          if (ps > 0) load_old(ps);
 #pragma unroll
           for (int c = 0; c < kHalf / 32; ++c) {
             uint32_t o[32];
@@ -577,7 +590,7 @@ __global__ void __launch_bounds__(384, 1)
           }
           __syncwarp();  // the next pass reuses the slice
         }
-        if (write) *lse_ptr = lse_new;
+        if (ok && write) *lse_ptr = lse_new;
       }
     }
   }
