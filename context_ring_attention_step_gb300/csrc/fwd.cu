@@ -183,6 +183,21 @@ __global__ void __launch_bounds__(384, 1)
           ++issued;
         }
       }
+      if constexpr (!kFused) {
+        // CTAs run one per SM and start in order, so CTA b + next_cta takes an
+        // SM about when this one ends: bring its Q tiles into L2 now, so its
+        // first QK waits on L2 rather than on HBM.
+        const long long nb = (long long)blockIdx.x + p.next_cta;
+        if (ok && p.next_cta > 0 && nb < (long long)gridDim.x) {
+          const FwdItem nx = p.items[nb / p.Hq];
+          const int nh = (int)(nb % p.Hq);
+          for (int qt = 0; qt < 2; ++qt) {
+            const int first = nx.q0 + 128 * qt;
+            if (first >= nx.q1) continue;
+            for (int hf = 0; hf < D / 64; ++hf) tma_prefetch_l2_3d(&tmQ, 64 * hf, nh, first);
+          }
+        }
+      }
       if (!ok) {  // drain this CTA's copies still in flight
         mbar_wait_drain(b_q, 0);
         for (int i = issued > C::kStages ? issued - C::kStages : 0; i < issued; ++i)
@@ -614,6 +629,13 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items * p.Hq;
   if (grid <= 0) return cudaSuccess;
+  FwdParams q = p;
+  if (!kFused) {  // one CTA per SM (shared memory): the stride to the CTA that follows on an SM
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    q.next_cta = sms;
+  }
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(384);
@@ -624,7 +646,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   attr[0].val.programmaticStreamSerializationAllowed = kFused ? 0 : 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, p);
+  return cudaLaunchKernelEx(&cfg, kern, tq, tk, tv, q);
 }
 
 }  // namespace

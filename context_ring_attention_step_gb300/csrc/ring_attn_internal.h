@@ -46,6 +46,7 @@ struct FwdParams {
   float* o_run;      // fp32 [T, Hq, D] running (normalised) output (ring-step launches)
   float* lse;        // fp32 [Hq, T] running log-sum-exp (natural log)
   int* status;       // workspace status word
+  int32_t next_cta;  // ring-step launches: CTAs resident at once (one per SM)
   // single launch over all ring steps: per-tile (start, range end) table and
   // the final output, written once (bf16 or fp32)
   const int2* tiles;
