@@ -19,6 +19,11 @@
 // from tensor memory.  Each Q tile's issuer runs PV(j) then S(j+1); the two
 // softmax warpgroups take turns, so one tile's softmax overlaps the other
 // tile's MMAs.
+// Epilogue traffic: each warp passes its 32 rows through its slice of its Q
+// tile's shared-memory buffer (idle once the tile's last QK is done), so every
+// global load and store of the running (or final) output covers whole rows.
+// The producer prefetches into L2 the Q tiles of the CTA that will follow
+// this one on the SM.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
 
