@@ -20,6 +20,7 @@ workload on the host cores (rank 0 only).
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
@@ -268,6 +269,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="long_128k")
+    ap.add_argument("--layout", default=None, choices=["zigzag", "contiguous"],
+                    help="override the workload's shard layout (same inputs)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-tokens", type=int, default=12288)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -277,6 +280,8 @@ def main():
 
     from workloads import workload
     wl = workload(args.workload)
+    if args.layout and args.layout != wl.layout:
+        wl = dataclasses.replace(wl, layout=args.layout, name="%s_%s" % (wl.name, args.layout))
     if args.impl == "reference":
         return run_reference(args, wl)
 
