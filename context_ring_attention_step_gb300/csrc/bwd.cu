@@ -196,6 +196,19 @@ __global__ void __launch_bounds__(512, 1)
         for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(sDO + hf * 16384, &tmDO, b_dofull, 64 * hf, h, q0);
         ++issued_do;
       }
+      {
+        // CTAs run one per SM and start in order, so CTA b + next_cta takes an
+        // SM about when this one ends: bring its K/V tile into L2 now.
+        const long long nb = (long long)blockIdx.x + p.next_cta;
+        if (ok && p.next_cta > 0 && nb < (long long)gridDim.x) {
+          const BwdItem nx = p.items[nb];
+          const int ng = nx.flags >> kHeadShift;
+          for (int hf = 0; hf < D / 64; ++hf) {
+            tma_prefetch_l2_3d(&tmK, 64 * hf, ng, nx.k0);
+            tma_prefetch_l2_3d(&tmV, 64 * hf, ng, nx.k0);
+          }
+        }
+      }
       if (!ok) {  // drain this CTA's copies still in flight
         mbar_wait_drain(b_kv, 0);
         for (int i = issued_q > 2 ? issued_q - 2 : 0; i < issued_q; ++i)
@@ -529,9 +542,14 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items;
   if (grid <= 0) return cudaSuccess;
+  BwdParams q = p;  // one CTA per SM (shared memory): the stride to the CTA that follows on an SM
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+  q.next_cta = sms;
   // (Overlapping consecutive backward ring steps, as the forward does, was
-  // measured 1 % slower: two query shards' dQ rows then share L2.)
-  kern<<<(unsigned)grid, 512, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, p);
+  // measured slower: two query shards' dQ rows then share L2.)
+  kern<<<(unsigned)grid, 512, BwdCfg<D>::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, q);
   return cudaGetLastError();
 }
 

@@ -66,6 +66,7 @@ struct BwdParams {
   float* dk_acc;       // fp32 [T, Hkv, D]
   float* dv_acc;       // fp32 [T, Hkv, D]
   int* status;
+  int32_t next_cta;    // CTAs resident at once (one per SM)
 };
 
 // Record `msg` as this thread's last error text and return `st`.
