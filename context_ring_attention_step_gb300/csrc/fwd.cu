@@ -201,6 +201,16 @@ __global__ void __launch_bounds__(384, 1)
             if (first >= nx.q1) continue;
             for (int hf = 0; hf < D / 64; ++hf) tma_prefetch_l2_3d(&tmQ, 64 * hf, nh, first);
           }
+          // and its first key/value tile
+          const bool r0 = ceil128(nx.kb0, nx.ke0) > 0;
+          if (r0 || ceil128(nx.kb1, nx.ke1) > 0) {
+            const int nk0 = r0 ? nx.kb0 : nx.kb1;
+            const int ng = nh / (p.Hq / p.Hkv);
+            for (int hf = 0; hf < D / 64; ++hf) {
+              tma_prefetch_l2_3d(&tmK, 64 * hf, ng, nk0);
+              tma_prefetch_l2_3d(&tmV, 64 * hf, ng, nk0);
+            }
+          }
         }
       }
       if (!ok) {  // drain this CTA's copies still in flight
