@@ -38,10 +38,13 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: after a max update P s
 // bf16 P have room to spare).
 constexpr float kSpecSumLimit = 65536.0f;
 
-template <int D>
+template <int D, bool kFused>
 struct FwdCfg {
   static constexpr int kTile = 128 * D * 2;  // bytes of one 128-row bf16 tile
-  static constexpr int kStages = D == 128 ? 4 : 8;
+  // K/V stages: a fifth stage at d = 128 fits in shared memory (225.5 KB) and
+  // helps the single launch (1250 -> 1262 TFLOP/s at 128K) but not the
+  // ring-step launches (1195 -> 1181), whose CTAs are short.
+  static constexpr int kStages = D == 128 ? (kFused ? 5 : 4) : 8;
   static constexpr int kQBytes = 2 * kTile;
   static constexpr int kKVBytes = kStages * kTile;
   static constexpr int kBarOff = kQBytes + kKVBytes;
@@ -73,7 +76,7 @@ template <int D, bool kFused>
 __global__ void __launch_bounds__(384, 1)
     ring_fwd_step_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = FwdCfg<D>;
+  using C = FwdCfg<D, kFused>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sQ = smem_u32(smem);
@@ -640,7 +643,8 @@ template <int D, bool kFused>
 cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv, const FwdParams& p,
                    int num_items, cudaStream_t stream) {
   auto kern = ring_fwd_step_kernel<D, kFused>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, FwdCfg<D>::kSmem);
+  constexpr int kSmem = FwdCfg<D, kFused>::kSmem;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
   if (e != cudaSuccess) return e;
   const long long grid = (long long)num_items * p.Hq;
   if (grid <= 0) return cudaSuccess;
@@ -654,7 +658,7 @@ cudaError_t launch(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorM
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3((unsigned)grid);
   cfg.blockDim = dim3(384);
-  cfg.dynamicSmemBytes = FwdCfg<D>::kSmem;
+  cfg.dynamicSmemBytes = kSmem;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
