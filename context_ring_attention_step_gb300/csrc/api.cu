@@ -19,6 +19,14 @@
 #include "../../include/ring_attn.h"
 #include "ring_attn_internal.h"
 
+namespace ra {
+// aux_kernels.cu: zero `header_bytes` at `header` and copy up to two work
+// lists (device-visible pinned host memory -> workspace); byte counts are
+// multiples of 16.
+cudaError_t launch_ws_init(void* header, size_t header_bytes, const void* src0, void* dst0, size_t bytes0,
+                          const void* src1, void* dst1, size_t bytes1, cudaStream_t stream);
+}  // namespace ra
+
 using ra::BwdItem;
 using ra::FwdItem;
 
@@ -36,6 +44,17 @@ struct ra_plan {
   std::vector<FwdItem> ffw;
   std::vector<int32_t> ftiles;
   int64_t visible_pairs = 0;
+  // The work lists again, in device-visible pinned host memory (each list
+  // padded to 16 bytes): a call's workspace set-up is then one small kernel
+  // on its stream, not a copy-engine transfer from pageable memory (which can
+  // block the host and queue behind the caller's own large copies).  Null
+  // where pinned memory is unavailable; the calls then copy from the vectors.
+  uint8_t* staged = nullptr;
+  const uint8_t* staged_dev = nullptr;
+  size_t st_fwd = 0, st_bwd = 0, st_ffw = 0, st_tiles = 0;
+  ~ra_plan() {
+    if (staged) cudaFreeHost(staged);
+  }
 };
 
 namespace {
@@ -328,6 +347,52 @@ bool encode_acc(CUtensorMap* m, const void* base, int T, int H, int D) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+size_t pad16(size_t b) { return (b + 15) & ~size_t(15); }
+
+// Copy the work lists into mapped pinned host memory (see ra_plan::staged).
+void stage_work_lists(ra_plan& P) {
+  const size_t bf = pad16(P.fwd.size() * sizeof(FwdItem)), bb = pad16(P.bwd.size() * sizeof(BwdItem));
+  const size_t bu = pad16(P.ffw.size() * sizeof(FwdItem)), bt = pad16(P.ftiles.size() * sizeof(int32_t));
+  const size_t total = bf + bb + bu + bt;
+  if (total == 0) return;
+  void* h = nullptr;
+  if (cudaHostAlloc(&h, total, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
+    (void)cudaGetLastError();  // no usable device here: the calls copy from the vectors
+    return;
+  }
+  void* d = nullptr;
+  if (cudaHostGetDevicePointer(&d, h, 0) != cudaSuccess) {
+    (void)cudaGetLastError();
+    cudaFreeHost(h);
+    return;
+  }
+  uint8_t* b = static_cast<uint8_t*>(h);
+  std::memset(b, 0, total);
+  P.st_fwd = 0;
+  P.st_bwd = bf;
+  P.st_ffw = bf + bb;
+  P.st_tiles = bf + bb + bu;
+  if (!P.fwd.empty()) std::memcpy(b + P.st_fwd, P.fwd.data(), P.fwd.size() * sizeof(FwdItem));
+  if (!P.bwd.empty()) std::memcpy(b + P.st_bwd, P.bwd.data(), P.bwd.size() * sizeof(BwdItem));
+  if (!P.ffw.empty()) std::memcpy(b + P.st_ffw, P.ffw.data(), P.ffw.size() * sizeof(FwdItem));
+  if (!P.ftiles.empty()) std::memcpy(b + P.st_tiles, P.ftiles.data(), P.ftiles.size() * sizeof(int32_t));
+  P.staged = b;
+  P.staged_dev = static_cast<const uint8_t*>(d);
+}
+
+// Zero the workspace's status header and put up to two work lists in place:
+// (staged offset, host copy, bytes, workspace offset) per list.
+cudaError_t ws_setup(const ra_plan* P, uint8_t* ws, cudaStream_t st, size_t so0, const void* h0, size_t b0,
+                     size_t d0, size_t so1 = 0, const void* h1 = nullptr, size_t b1 = 0, size_t d1 = 0) {
+  if (P->staged_dev)
+    return ra::launch_ws_init(ws, kHeader, P->staged_dev + so0, ws + d0, b0 ? pad16(b0) : 0, P->staged_dev + so1,
+                              ws + d1, b1 ? pad16(b1) : 0, st);
+  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
+  if (e == cudaSuccess && b0) e = cudaMemcpyAsync(ws + d0, h0, b0, cudaMemcpyHostToDevice, st);
+  if (e == cudaSuccess && b1) e = cudaMemcpyAsync(ws + d1, h1, b1, cudaMemcpyHostToDevice, st);
+  return e;
+}
+
 ra_status cuda_fail(cudaError_t e, const char* what) {
   return fail(RA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
@@ -397,6 +462,7 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
   }
   build_items(*P);
   build_fused(*P);
+  stage_work_lists(*P);
   *out = P;
   return RA_OK;
 }
@@ -475,12 +541,8 @@ ra_status ra_fwd_prepare(const ra_plan* P, int32_t o_is_fp32, void* workspace, s
   if (rs != RA_OK) return rs;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
-  if (e != cudaSuccess) return cuda_fail(e, "status reset");
-  if (!P->fwd.empty()) {
-    e = cudaMemcpyAsync(ws + L.items, P->fwd.data(), P->fwd.size() * sizeof(FwdItem), cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(e, "work-list copy");
-  }
+  cudaError_t e = ws_setup(P, ws, st, P->st_fwd, P->fwd.data(), P->fwd.size() * sizeof(FwdItem), L.items);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace set-up");
   return RA_OK;
 }
 
@@ -579,13 +641,10 @@ ra_status ra_fwd_fused(const ra_plan* P, const void* q, const void* k, const voi
     return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", workspace_bytes, L.total);
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
-  if (e != cudaSuccess) return cuda_fail(e, "status reset");
+  cudaError_t e = ws_setup(P, ws, st, P->st_ffw, P->ffw.data(), P->ffw.size() * sizeof(FwdItem), L.items,
+                           P->st_tiles, P->ftiles.data(), P->ftiles.size() * sizeof(int32_t), L.tiles);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace set-up");
   if (P->ffw.empty()) return RA_OK;
-  e = cudaMemcpyAsync(ws + L.items, P->ffw.data(), P->ffw.size() * sizeof(FwdItem), cudaMemcpyHostToDevice, st);
-  if (e == cudaSuccess)
-    e = cudaMemcpyAsync(ws + L.tiles, P->ftiles.data(), P->ftiles.size() * sizeof(int32_t), cudaMemcpyHostToDevice, st);
-  if (e != cudaSuccess) return cuda_fail(e, "work-list copy");
   CUtensorMap tq, tk, tv;
   if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
       !encode_thd(&tv, v, P->T, P->Hkv, P->D))
@@ -651,12 +710,8 @@ ra_status ra_bwd_prepare(const ra_plan* P, const void* o, int32_t o_is_fp32, con
     return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaError_t e = cudaMemsetAsync(ws, 0, kHeader, st);
-  if (e != cudaSuccess) return cuda_fail(e, "status reset");
-  if (!P->bwd.empty()) {
-    e = cudaMemcpyAsync(ws + L.items, P->bwd.data(), P->bwd.size() * sizeof(BwdItem), cudaMemcpyHostToDevice, st);
-    if (e != cudaSuccess) return cuda_fail(e, "work-list copy");
-  }
+  cudaError_t e = ws_setup(P, ws, st, P->st_bwd, P->bwd.data(), P->bwd.size() * sizeof(BwdItem), L.items);
+  if (e != cudaSuccess) return cuda_fail(e, "workspace set-up");
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
   // the row padding past T is read by the tile loads (and masked): keep it finite
   e = cudaMemsetAsync(ws + L.delta, 0, L.dq ? L.dq - L.delta : L.total - L.delta, st);

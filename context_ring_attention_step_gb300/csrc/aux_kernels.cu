@@ -4,6 +4,8 @@
 //     reductions, and LSE rescaled to log2 units for the exp2-based recompute.
 #include <cuda_bf16.h>
 
+#include <algorithm>
+
 #include "ring_attn_internal.h"
 #include "tc.cuh"
 
@@ -37,6 +39,18 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 }
 
 // n8 = number of 8-element groups
+// Workspace set-up without the copy engines: zero the status header and copy
+// up to two work lists from mapped pinned host memory (read over the host
+// link by the SMs).  Sizes are multiples of 16 bytes.
+__global__ void ws_init_kernel(uint4* __restrict__ header, int header16, const uint4* __restrict__ src0,
+                               uint4* __restrict__ dst0, size_t n0, const uint4* __restrict__ src1,
+                               uint4* __restrict__ dst1, size_t n1) {
+  const size_t tid = blockIdx.x * (size_t)blockDim.x + threadIdx.x, stride = (size_t)gridDim.x * blockDim.x;
+  if (tid < (size_t)header16) header[tid] = make_uint4(0u, 0u, 0u, 0u);
+  for (size_t i = tid; i < n0; i += stride) dst0[i] = src0[i];
+  for (size_t i = tid; i < n1; i += stride) dst1[i] = src1[i];
+}
+
 __global__ void cast_bf16_kernel(const float4* __restrict__ src, uint4* __restrict__ dst, size_t n8) {
   for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
     const float4 a = __ldcs(src + 2 * i);
@@ -108,6 +122,18 @@ cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t
   const unsigned blocks = (unsigned)(want < 152 * 16 ? want : 152 * 16);
   cast_bf16_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<const float4*>(src),
                                                     reinterpret_cast<uint4*>(dst), n8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ws_init(void* header, size_t header_bytes, const void* src0, void* dst0, size_t bytes0,
+                          const void* src1, void* dst1, size_t bytes1, cudaStream_t stream) {
+  const size_t n0 = bytes0 / 16, n1 = bytes1 / 16, most = std::max(std::max(n0, n1), header_bytes / 16);
+  const int threads = 256;
+  const unsigned blocks = (unsigned)std::min<size_t>(std::max<size_t>((most + threads - 1) / threads, 1), 152);
+  ws_init_kernel<<<blocks, threads, 0, stream>>>(reinterpret_cast<uint4*>(header), (int)(header_bytes / 16),
+                                                  reinterpret_cast<const uint4*>(src0), reinterpret_cast<uint4*>(dst0),
+                                                  n0, reinterpret_cast<const uint4*>(src1),
+                                                  reinterpret_cast<uint4*>(dst1), n1);
   return cudaGetLastError();
 }
 

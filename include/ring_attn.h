@@ -94,13 +94,17 @@ int32_t ra_abi_version(void);
  *   num_q_heads, num_kv_heads: Hq % Hkv == 0.
  *   softmax_scale   <= 0 selects 1/sqrt(head_dim).
  * The plan copies what it needs; the caller's arrays may be freed afterwards.
+ * Where a CUDA device is usable, the plan also keeps its work lists in mapped
+ * pinned host memory (cudaHostAlloc, a host allocation) so that each call
+ * sets up its workspace with one small kernel instead of a copy from pageable
+ * memory; without a device the plan is host-only and the calls copy.
  */
 ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_docs,
                          const int32_t* cp_size_per_doc, int32_t cp_size, int32_t layout,
                          int32_t causal, int32_t num_q_heads, int32_t num_kv_heads,
                          int32_t head_dim, float softmax_scale);
 
-/* Free a plan (NULL is ignored). */
+/* Free a plan (NULL is ignored), including its pinned work-list copy. */
 void ra_plan_destroy(ra_plan* plan);
 
 /*
