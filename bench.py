@@ -529,7 +529,10 @@ def main():
             "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
             "useful_flops_per_step": ff + fb, "strict_bwd_flops_per_step": 0.8 * fb,
             "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "single_launch_forward": fused,
-            "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3),
+            # per step: the ring steps, the output cast, the backward preprocess,
+            # the three gradient casts and the two workspace set-up kernels (one
+            # per prepare; a plan without pinned work lists copies instead)
+            "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3 + 2),
             "clocks": clk.summary(),
         }
         print(json.dumps(line))
