@@ -10,6 +10,7 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -355,6 +356,8 @@ void stage_work_lists(ra_plan& P) {
   const size_t bu = pad16(P.ffw.size() * sizeof(FwdItem)), bt = pad16(P.ftiles.size() * sizeof(int32_t));
   const size_t total = bf + bb + bu + bt;
   if (total == 0) return;
+  const char* off = std::getenv("RA_NO_PINNED_WORK_LISTS");  // tests of the copy fallback
+  if (off && off[0] == '1') return;
   void* h = nullptr;
   if (cudaHostAlloc(&h, total, cudaHostAllocMapped | cudaHostAllocPortable) != cudaSuccess) {
     (void)cudaGetLastError();  // no usable device here: the calls copy from the vectors

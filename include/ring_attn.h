@@ -97,7 +97,8 @@ int32_t ra_abi_version(void);
  * Where a CUDA device is usable, the plan also keeps its work lists in mapped
  * pinned host memory (cudaHostAlloc, a host allocation) so that each call
  * sets up its workspace with one small kernel instead of a copy from pageable
- * memory; without a device the plan is host-only and the calls copy.
+ * memory; without a device the plan is host-only and the calls copy.  The
+ * environment variable RA_NO_PINNED_WORK_LISTS=1 selects the copies (tests).
  */
 ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_docs,
                          const int32_t* cp_size_per_doc, int32_t cp_size, int32_t layout,

@@ -191,3 +191,29 @@ def test_autograd_wrapper_matches_explicit_calls(ra):
     for a, b in zip((qa.grad, ka.grad, va.grad), g_ref):
         assert a.dtype == b.dtype and a.shape == b.shape
         assert torch.allclose(a.float(), b.float(), rtol=2 ** -7, atol=1e-5)
+
+
+def test_work_list_copy_fallback_matches(ra, monkeypatch):
+    """A plan built without pinned work lists (the calls then copy them with
+    cudaMemcpyAsync) gives the same forward and backward as the default plan,
+    whose calls set up the workspace with a kernel."""
+    wl = custom([900, 333], 4, 2, 128, 3, "zigzag", True, seed=35, name="ws_setup")
+    q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
+    cps = list(wl.cp_per_doc)
+    args = (wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale)
+    mk = lambda: ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    staged = mk()
+    monkeypatch.setenv("RA_NO_PINNED_WORK_LISTS", "1")
+    copied = mk()
+    monkeypatch.delenv("RA_NO_PINNED_WORK_LISTS")
+    outs = []
+    for plan in (staged, copied):
+        o, lse = ra.ring_attn_fwd(q, k, v, *args, o_fp32=True, plan=plan, check=True)
+        o_f, lse_f = ra.ring_attn_fwd(q, k, v, *args, plan=plan, check=True, fused=True)
+        g = ra.ring_attn_bwd(q, k, v, o, do, lse, *args, grads_fp32=True, plan=plan, check=True)
+        outs.append((o, lse, o_f, lse_f) + tuple(g))
+    torch.cuda.synchronize()
+    for a, b in zip(outs[0][:4], outs[1][:4]):
+        assert torch.equal(a, b)  # the forward has no atomics
+    for a, b in zip(outs[0][4:], outs[1][4:]):
+        assert torch.allclose(a, b, rtol=1e-4, atol=1e-5)  # dQ is summed with atomic adds
