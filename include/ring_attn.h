@@ -42,10 +42,12 @@
  * Every device pointer must be 16-byte aligned.  head_dim is 64 or 128.
  *
  * Ownership: the caller owns every device buffer, including the workspace.
- * The plan is host memory only (it never touches the GPU).  ra_fwd/ra_bwd
- * copy the plan's work lists into the workspace with cudaMemcpyAsync, enqueue
- * kernels on `stream` (a cudaStream_t, NULL = legacy default stream) and
- * return without synchronising; nothing is allocated on the device.
+ * The plan is host memory (its work lists are also kept in mapped pinned host
+ * memory where a device is usable; see ra_plan_create).  ra_fwd/ra_bwd put the
+ * plan's work lists into the workspace (a small kernel reading the pinned
+ * copy, else cudaMemcpyAsync), enqueue kernels on `stream` (a cudaStream_t,
+ * NULL = legacy default stream) and return without synchronising; nothing is
+ * allocated on the device.
  *
  * Errors: every entry point validates its arguments on the host first and
  * returns RA_ERR_INVALID_ARG / RA_ERR_UNSUPPORTED / RA_ERR_WORKSPACE before
@@ -77,7 +79,7 @@ typedef enum {
 typedef enum { RA_LAYOUT_CONTIGUOUS = 0, RA_LAYOUT_ZIGZAG = 1 } ra_layout;
 typedef enum { RA_CP_DYNAMIC = 0, RA_CP_STATIC = 1 } ra_cp_mode;
 
-typedef struct ra_plan ra_plan; /* opaque, host memory only */
+typedef struct ra_plan ra_plan; /* opaque, host memory (work lists also pinned) */
 
 /* Version of this ABI (bumped on any signature change). */
 int32_t ra_abi_version(void);
