@@ -43,3 +43,28 @@ def test_single_process_is_identity():
     import bench
     assert bench.max_over_ranks(12.5) == 12.5
     assert bench.whole_job_tflops(1, 1e12, 1, 1000.0) == pytest.approx(1.0)
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the fp64 oracle on the host cores) prints
+    one JSON line with the contract's keys; it needs no GPU."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny", "--steps", "1",
+                        "--warmup", "1", "--cpu-tokens", "512"], cwd=root, capture_output=True, text=True,
+                       timeout=600)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "TFLOP/s"
+    assert d["n_gpus"] == 1 and d["steps"] == 1 and d["warmup"] >= 3 and d["higher_is_better"] is True
+    assert d["scaling"] == "weak" and d["vs_baseline"] is None and d["data"] == "synthetic"
+    assert d["config"]["workload"] == "tiny"
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["sample"] and cb["value"] == d["value"]
+    e = d["e2e"]
+    assert e["value"] == d["value"] and e["unit"] == d["unit"]
+    assert e["h2d_bytes_per_step"] == 0 and e["d2h_bytes_per_step"] == 0
