@@ -272,7 +272,8 @@ def main():
     ap.add_argument("--layout", default=None, choices=["zigzag", "contiguous"],
                     help="override the workload's shard layout (same inputs)")
     ap.add_argument("--e2e-steps", type=int, default=8)
-    ap.add_argument("--cpu-tokens", type=int, default=12288)
+    # ~12 s of fp64 oracle work per sample on a 16-core host at the 128K shape
+    ap.add_argument("--cpu-tokens", type=int, default=40960)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.warmup < 3:
