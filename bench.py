@@ -302,7 +302,9 @@ def main():
 
     q_h, k_h, v_h, do_h = draw_qkvdo(wl)
     cps = list(wl.cp_per_doc)
+    t_plan = time.perf_counter()
     plan = ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan_ms = (time.perf_counter() - t_plan) * 1e3  # host, once per batch layout; not in the timed region
     steps = plan.stats()["steps"]
     q, k, v, do = (x.to(dev) for x in (q_h, k_h, v_h, do_h))
     T, Hq, Hkv, D = wl.T, wl.Hq, wl.Hkv, wl.d
@@ -534,6 +536,7 @@ def main():
             # the three gradient casts and the two workspace set-up kernels (one
             # per prepare; a plan without pinned work lists copies instead)
             "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3 + 2),
+            "plan_ms": plan_ms,
             "clocks": clk.summary(),
         }
         print(json.dumps(line))
