@@ -236,3 +236,31 @@ def test_fused_forward_tiles_cover_each_visible_pair_once(ra, layout, causal, le
     assert set(got) == want
     assert rows == set(range(wl.T))
     assert plan.fused_workspace_bytes() >= 256 + 32 * len(items) + 8 * len(tiles)
+
+
+def test_python_api_has_no_cpu_path(ra):
+    """The binding computes nothing itself: CPU tensors are refused (no silent
+    fallback), for the forward, the backward and the autograd wrapper."""
+    import torch
+    T, H, D = 256, 2, 64
+    q = torch.zeros((T, H, D), dtype=torch.bfloat16)
+    lse = torch.zeros((H, T), dtype=torch.float32)
+    args = ([0, T], 2, "zigzag", True)
+    with pytest.raises(ValueError, match="CUDA"):
+        ra.ring_attn_fwd(q, q, q, *args)
+    with pytest.raises(ValueError, match="CUDA"):
+        ra.ring_attn_bwd(q, q, q, q, q, lse, *args)
+    with pytest.raises(ValueError, match="CUDA"):
+        ra.ring_attention(q, q, q, *args)
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    """A missing shared library is an error, not a fallback."""
+    import context_ring_attention_step_gb300.ring_attn as m
+    saved = m._lib
+    try:
+        m._lib = None
+        with pytest.raises(RuntimeError, match="not found"):
+            m.load_library(str(tmp_path / "absent.so"))
+    finally:
+        m._lib = saved
