@@ -3,10 +3,12 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step = the whole hot path on one batch: ring forward (all ring steps,
-exact log-sum-exp merge, bf16 output) then ring backward (Delta preprocess,
-all ring steps, bf16 gradients), on seeded synthetic bf16 inputs resident in
-HBM.  Useful FLOPs count visible (query, key) pairs only: forward 4 d Hq P,
+One step = the whole hot path on one batch: ring forward (every ring step in
+one launch, the merge of each step into the running state kept on chip, bf16
+output; ra_fwd) then ring backward (Delta preprocess, one launch per ring
+step, bf16 gradients; ra_bwd's calls), on seeded synthetic bf16 inputs
+resident in HBM.  The forward with one launch per ring step (merge through
+HBM) is timed beside it and reported as ring_step_forward.  Useful FLOPs count visible (query, key) pairs only: forward 4 d Hq P,
 backward 10 d Hq P (P = sum over documents of L(L+1)/2 when causal).
 
 With N > 1 (torchrun, one process per GPU) every rank runs an independent
@@ -220,6 +222,69 @@ def cpu_oracle_sample(wl, q, k, v, do, tokens):
     return flops, dt, "causal prefix of %d tokens of document 0, query head 0 / kv head 0, fwd+bwd in float64" % Tn
 
 
+def cpu_parity_sample(wl, q, k, v, do, o, lse, dq, dk, dv, nrows=16):
+    """Max abs errors of the bench's own outputs (bf16 O, dQ, dK, dV; fp32 LSE)
+    against the fp64 oracle on a sample that the oracle computes exactly one
+    output at a time: O, LSE and dQ of sampled query rows (random rows plus
+    every document's first and last row) of the first and last query heads,
+    and, under a causal mask, dK and dV of the last 128 keys of the longest
+    document for the first and last key/value heads."""
+    import numpy as np
+    from oracle import attention as A
+    G = wl.Hq // wl.Hkv
+    cu = wl.cu_seqlens
+    rng = np.random.default_rng(wl.seed)
+    rows = set(rng.integers(0, wl.T, nrows).tolist())
+    for d in range(wl.num_docs):
+        if cu[d + 1] > cu[d]:
+            rows.update({cu[d], cu[d + 1] - 1})
+    rows = sorted(rows)
+    err = {"o": 0.0, "lse": 0.0, "dq": 0.0, "dk": 0.0, "dv": 0.0}
+    excess = -1.0  # max over outputs of |err| - bound (<= 0: within the bounds)
+    ridx = torch_index(rows)
+    for h in (0, wl.Hq - 1):
+        g = h // G
+        qh, dh = q[:, h:h + 1].contiguous(), do[:, h:h + 1].contiguous()
+        kh, vh = k[:, g:g + 1].contiguous(), v[:, g:g + 1].contiguous()
+        ro, rl = A.attention_rows(qh, kh, vh, cu, rows, 0, wl.causal, wl.softmax_scale)
+        rdq = A.attention_rows_dq(qh, kh, vh, dh, cu, rows, 0, wl.causal, wl.softmax_scale)
+        go = o[ridx, h].float().cpu().numpy()
+        gl = lse[h, ridx].cpu().numpy()
+        gq = dq[ridx, h].float().cpu().numpy()
+        for name, x, r in (("o", go, ro), ("dq", gq, rdq)):
+            e = np.abs(x - r)
+            err[name] = max(err[name], float(e.max()))
+            excess = max(excess, float((e - (2e-2 + np.abs(r) * 2.0 ** -9)).max()))
+        err["lse"] = max(err["lse"], float(np.abs(gl - rl).max()))
+        excess = max(excess, err["lse"] - 1e-3)
+    what = "O, LSE, dQ of %d query rows of query heads 0 and %d" % (len(rows), wl.Hq - 1)
+    if wl.causal:
+        longest = max(range(wl.num_docs), key=lambda d: cu[d + 1] - cu[d])
+        keys = list(range(max(cu[longest], cu[longest + 1] - 128), cu[longest + 1]))
+        kidx = torch_index(keys)
+        for g in (0, wl.Hkv - 1):
+            hs = slice(g * G, (g + 1) * G)
+            rk, rv = A.attention_keys_dkdv(q[:, hs].contiguous(), k[:, g:g + 1].contiguous(),
+                                           v[:, g:g + 1].contiguous(), do[:, hs].contiguous(), cu, keys, 0,
+                                           True, wl.softmax_scale)
+            for name, x, r in (("dk", dk[kidx, g], rk), ("dv", dv[kidx, g], rv)):
+                e = np.abs(x.float().cpu().numpy() - r)
+                err[name] = max(err[name], float(e.max()))
+                excess = max(excess, float((e - (2e-2 + np.abs(r) * 2.0 ** -9)).max()))
+        what += "; dK, dV of the last %d keys of document %d, kv heads 0 and %d" % (len(keys), longest,
+                                                                                   wl.Hkv - 1)
+    else:
+        err["dk"] = err["dv"] = None
+    return {"max_abs_err": err, "within_bounds": excess <= 0, "sample": what,
+            "bounds": "2e-2 + 2^-9 |ref| on the bf16 outputs O, dQ, dK, dV; 1e-3 on LSE",
+            "outputs": "the bench's last timed step (bf16 O and gradients)"}
+
+
+def torch_index(idx):
+    import torch
+    return torch.tensor(idx, dtype=torch.long)
+
+
 def blas_threads():
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         if os.environ.get(var):
@@ -331,29 +396,29 @@ def main():
         if st != 0:
             raise RuntimeError("ring_attn status %d: %s" % (st, lib.ra_last_error().decode()))
 
-    def events():
-        return [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    def new_event():
+        return torch.cuda.Event(enable_timing=True)
 
-    # Events bracket each pass's ring-step launches as a whole (an event between
-    # two launches would stop the next ring step from starting on the SMs the
-    # previous one frees).
-    def one_step(ev_f=None, ev_b=None):
-        chk(lib.ra_fwd_prepare(H, 0, P_(ws_f), wf, sp))
-        if ev_f:
-            ev_f[0].record(stream)
-        for s in range(steps):
-            chk(lib.ra_fwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(o), 0, P_(lse), P_(ws_f), wf, sp))
-        if ev_f:
-            ev_f[1].record(stream)
-        chk(lib.ra_fwd_finish(H, P_(o), 0, P_(ws_f), wf, sp))
+    # One step: the forward (the whole ring in one launch, ra_fwd), then the
+    # backward (Delta preprocess, one launch per ring step, gradient casts).
+    # Events mark the start of the step, the end of the forward and the span
+    # of the backward ring-step launches (an event between two ring-step
+    # launches would stop the next one from starting on the SMs the previous
+    # one frees, so the backward's launches are bracketed as a whole).
+    def one_step(ev=None):
+        if ev:
+            ev["start"].record(stream)
+        chk(lib.ra_fwd(H, P_(q), P_(k), P_(v), P_(o), 0, P_(lse), P_(ws_f), wf, sp))
+        if ev:
+            ev["fwd"].record(stream)
         chk(lib.ra_bwd_prepare(H, P_(o), 0, P_(do), P_(lse), P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb, sp))
-        if ev_b:
-            ev_b[0].record(stream)
+        if ev:
+            ev["bwd0"].record(stream)
         for s in range(steps):
             chk(lib.ra_bwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(do), P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb,
                                      sp))
-        if ev_b:
-            ev_b[1].record(stream)
+        if ev:
+            ev["bwd1"].record(stream)
         chk(lib.ra_bwd_finish(H, P_(dq), P_(dk), P_(dv), 0, P_(ws_b), wb, sp))
 
     for _ in range(args.warmup):
@@ -363,47 +428,56 @@ def main():
     chk(lib.ra_workspace_status(P_(ws_b), sp))
 
     # ---------------------------------------------------------------- timed region
-    t_f = [0.0] * steps
-    t_b = [0.0] * steps
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0, e1 = new_event(), new_event()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
-    evs = [(events(), events()) for _ in range(args.steps)]
+    evs = [{n: new_event() for n in ("start", "fwd", "bwd0", "bwd1")} for _ in range(args.steps)]
     with ClockSampler(local) as clk:
         e0.record(stream)
         for it in range(args.steps):
-            one_step(*evs[it])
+            one_step(evs[it])
         e1.record(stream)
         torch.cuda.synchronize()
-    for ev_f, ev_b in evs:
-        t_f[0] += ev_f[0].elapsed_time(ev_f[1])
-        t_b[0] += ev_b[0].elapsed_time(ev_b[1])
     ms_total = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     if world > 1:
         dist.barrier()
     chk(lib.ra_workspace_status(P_(ws_f), sp))
     chk(lib.ra_workspace_status(P_(ws_b), sp))
+    step_ms = [evs[i]["start"].elapsed_time(evs[i + 1]["start"] if i + 1 < args.steps else e1)
+               for i in range(args.steps)]
+    t_f = [ev["start"].elapsed_time(ev["fwd"]) for ev in evs]
+    t_b = [ev["bwd0"].elapsed_time(ev["bwd1"]) for ev in evs]
 
-    # ---------------------------------------------------------------- single-launch forward
-    # The same forward with the whole ring in one launch (ra_fwd_fused): timed
-    # after the ring-step region, on its own output buffers.
-    fused = None
-    wfu = plan.fused_workspace_bytes()
-    ws_u = torch.empty(wfu, dtype=torch.uint8, device=dev)
-    o_u = torch.empty_like(o)
-    lse_u = torch.empty_like(lse)
+    # ---------------------------------------------------------------- ring-step forward
+    # The same forward with one launch per ring step and the merge into a
+    # running (O, LSE) in HBM (ra_fwd_ring_steps, the per-step unit a
+    # multi-GPU driver would interleave with its KV exchanges): timed after the
+    # main region, on its own output buffers.
+    wrs = plan.ring_step_workspace_bytes(False)
+    ws_r = torch.empty(wrs, dtype=torch.uint8, device=dev)
+    o_r = torch.empty_like(o)
+    lse_r = torch.empty_like(lse)
+
+    def ring_step_fwd(ev=None):
+        chk(lib.ra_fwd_prepare(H, 0, P_(ws_r), wrs, sp))
+        if ev:
+            ev[0].record(stream)
+        for s in range(steps):
+            chk(lib.ra_fwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(o_r), 0, P_(lse_r), P_(ws_r), wrs, sp))
+        if ev:
+            ev[1].record(stream)
+        chk(lib.ra_fwd_finish(H, P_(o_r), 0, P_(ws_r), wrs, sp))
+
     for _ in range(max(1, args.warmup)):
-        chk(lib.ra_fwd_fused(H, P_(q), P_(k), P_(v), P_(o_u), 0, P_(lse_u), P_(ws_u), wfu, sp))
+        ring_step_fwd()
     torch.cuda.synchronize()
-    u0, u1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    u0.record(stream)
-    for _ in range(args.steps):
-        chk(lib.ra_fwd_fused(H, P_(q), P_(k), P_(v), P_(o_u), 0, P_(lse_u), P_(ws_u), wfu, sp))
-    u1.record(stream)
+    rev = [(new_event(), new_event()) for _ in range(args.steps)]
+    for it in range(args.steps):
+        ring_step_fwd(rev[it])
     torch.cuda.synchronize()
-    chk(lib.ra_workspace_status(P_(ws_u), sp))
-    fused_ms = max_over_ranks(u0.elapsed_time(u1), dist, dev) / args.steps
+    chk(lib.ra_workspace_status(P_(ws_r), sp))
+    rs_kernel_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in rev), dist, dev) / args.steps
 
     ff, fb = useful_flops(wl)
     ms_step = ms_total / args.steps
@@ -411,26 +485,38 @@ def main():
     peak_b, peak_s, hbm, peak_kind = peaks()
     fwd_ms = sum(t_f) / args.steps
     bwd_ms = sum(t_b) / args.steps
-    fused = {"fwd_ms": fused_ms, "fwd_tflops": ff / (fused_ms * 1e-3) / 1e12,
-             "fwd_plus_ring_step_bwd_tflops": world * (ff + fb) / ((fused_ms + bwd_ms) * 1e-3) / 1e12,
-             "note": "forward with the whole ring in one launch (running state kept on chip); "
-                     "timed separately, not part of value"}
+    ring_steps = {"fwd_kernels_ms": rs_kernel_ms, "fwd_tflops": ff / (rs_kernel_ms * 1e-3) / 1e12,
+                  "launches": fwd_launches,
+                  "note": "forward with one launch per ring step (ra_fwd_ring_steps), timed separately over "
+                          "its ring-step launches; not part of value"}
 
-    # roofline of the dominant kernel (per-launch events on the launching stream)
-    if sum(t_b) >= sum(t_f):
-        name, tot_ms, launches, pairs, per_pair = "ring_bwd_step_kernel", sum(t_b), bwd_launches, bpairs, 10.0
-    else:
-        name, tot_ms, launches, pairs, per_pair = "ring_fwd_step_kernel", sum(t_f), fwd_launches, fpairs, 4.0
-    alg_flops_per_launch = per_pair * wl.d * wl.Hq * sum(pairs) / max(1, launches)
-    avg_launch_s = tot_ms * 1e-3 / (args.steps * max(1, launches))
-    achieved = alg_flops_per_launch / avg_launch_s / 1e12
-    roof = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak_s, "unit": "TFLOP/s",
-            "frac": achieved / peak_s, "peak_kind": peak_kind + " bf16 sustained (kernel timed inside a long step)",
-            "frac_of_burst_peak": achieved / peak_b, "traffic": recorded_traffic(name, wl.name),
-            "traffic_unit": "bytes per launch (dram read + write, ncu)",
-            "per_launch_flops": alg_flops_per_launch, "avg_launch_ms": avg_launch_s * 1e3,
-            "timing": "CUDA events on the launching stream around each pass's ring-step launches "
-                      "(launches of a pass may overlap: programmatic dependent launch); average = pass / launches"}
+    # roofline of the dominant kernel (events on the launching stream)
+    bwd_alg = 10.0 * wl.d * wl.Hq * sum(bpairs) / max(1, bwd_launches)
+    bwd_launch_s = sum(t_b) * 1e-3 / (args.steps * max(1, bwd_launches))
+    fwd_alg = ff  # the single-launch forward: one launch per step does the whole forward
+    fwd_launch_s = sum(t_f) * 1e-3 / args.steps
+    kernels = {
+        "ring_bwd_step_kernel": (bwd_alg, bwd_launch_s, sum(t_b),
+                                 "CUDA events on the launching stream around each step's backward ring-step "
+                                 "launches (one kernel per ring step); average = span / launches"),
+        "ring_fwd_step_kernel (single launch)": (fwd_alg, fwd_launch_s, sum(t_f),
+                                                 "CUDA events on the launching stream around ra_fwd "
+                                                 "(work-list set-up kernel + the forward kernel)"),
+    }
+    roofs = {}
+    for name, (alg, launch_s, _, how) in kernels.items():
+        achieved = alg / launch_s / 1e12
+        roofs[name] = {"kernel": name, "bound": "tensor", "achieved": achieved, "peak": peak_s,
+                       "unit": "TFLOP/s", "frac": achieved / peak_s,
+                       "peak_kind": peak_kind + " bf16 sustained (kernel timed inside a long step)",
+                       "frac_of_burst_peak": achieved / peak_b,
+                       "traffic": recorded_traffic(name.split(" ")[0], wl.name) if name.startswith("ring_bwd")
+                       else None,
+                       "traffic_unit": "bytes per launch (dram read + write, ncu)",
+                       "per_launch_flops": alg, "avg_launch_ms": launch_s * 1e3, "timing": how}
+    dominant = max(kernels, key=lambda n: kernels[n][2])
+    roof = roofs[dominant]
+    roof_other = {n: r for n, r in roofs.items() if n != dominant}
 
     # ---------------------------------------------------------------- end to end (host buffers)
     # Every step copies its inputs from pinned host memory and its results back
@@ -514,11 +600,14 @@ def main():
                "ms_per_step": e_ms / args.e2e_steps, "warmup": 2,
                "copies": "pinned host <-> device, uploads and downloads on two streams, double-buffered device inputs and outputs (no allocation in the timed loop), overlapping compute"}
 
-    cpu = None
+    # CPU leg (rank 0, one GPU): the oracle timed on a bounded sample, and the
+    # bench's own outputs checked against it on sampled rows and keys
+    cpu, parity = None, None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         flops, dt, sample = cpu_oracle_sample(wl, q_h, k_h, v_h, do_h, args.cpu_tokens)
         cpu = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": blas_threads(), "kind": "oracle",
                "sample": sample, "seconds": dt}
+        parity = cpu_parity_sample(wl, q_h, k_h, v_h, do_h, o, lse, dq, dk, dv)
 
     if rank == 0:
         line = {
@@ -527,15 +616,19 @@ def main():
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic", "config": config_of(wl),
             "pct_of_bf16_peak": 100.0 * value / world / peak_b, "pct_of_bf16_peak_sustained":
                 100.0 * value / world / peak_s,
-            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+            "ms_per_step_median": statistics.median(step_ms), "ms_per_step_mean": statistics.mean(step_ms),
+            "ms_per_step_all": step_ms,
+            "fwd_ms": fwd_ms, "bwd_ms": bwd_ms, "bwd_with_preprocess_and_casts_ms": ms_step - fwd_ms,
             "fwd_tflops": ff / (fwd_ms * 1e-3) / 1e12 if fwd_ms else None,
             "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
             "useful_flops_per_step": ff + fb, "strict_bwd_flops_per_step": 0.8 * fb,
-            "roofline": roof, "cpu_baseline": cpu, "e2e": e2e, "single_launch_forward": fused,
-            # per step: the ring steps, the output cast, the backward preprocess,
-            # the three gradient casts and the two workspace set-up kernels (one
-            # per prepare; a plan without pinned work lists copies instead)
-            "gpu_launches": args.steps * (fwd_launches + 1 + 1 + bwd_launches + 3 + 2),
+            "roofline": roof, "roofline_other_kernels": roof_other, "cpu_baseline": cpu,
+            "parity_vs_oracle": parity, "e2e": e2e, "ring_step_forward": ring_steps,
+            # per step: the forward's work-list set-up and forward kernel, the
+            # backward's work-list set-up and Delta preprocess, its ring steps
+            # and the three gradient casts (a plan without pinned work lists
+            # copies its work lists instead of running the set-up kernels)
+            "gpu_launches": args.steps * (2 + 2 + bwd_launches + 3),
             "plan_ms": plan_ms,
             "clocks": clk.summary(),
         }

@@ -411,7 +411,7 @@ ra_status set_last_error(ra_status st, const char* msg) {
 
 extern "C" {
 
-int32_t ra_abi_version(void) { return 1; }
+int32_t ra_abi_version(void) { return 2; }
 
 const char* ra_last_error(void) { return g_err.c_str(); }
 
@@ -475,8 +475,16 @@ void ra_plan_destroy(ra_plan* plan) { delete plan; }
 ra_status ra_plan_workspace_bytes(const ra_plan* P, int32_t o_is_fp32, int32_t grads_fp32, size_t* fwd_bytes,
                                   size_t* bwd_bytes) {
   if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
-  if (fwd_bytes) *fwd_bytes = fwd_layout(*P, o_is_fp32).total;
+  (void)o_is_fp32;  // ra_fwd writes its output once, in its final dtype: no running output
+  if (fwd_bytes) *fwd_bytes = fused_layout(*P).total;
   if (bwd_bytes) *bwd_bytes = bwd_layout(*P, grads_fp32).total;
+  return RA_OK;
+}
+
+ra_status ra_plan_ring_step_workspace_bytes(const ra_plan* P, int32_t o_is_fp32, size_t* fwd_bytes) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  if (!fwd_bytes) return fail(RA_ERR_INVALID_ARG, "fwd_bytes is NULL");
+  *fwd_bytes = fwd_layout(*P, o_is_fp32).total;
   return RA_OK;
 }
 
@@ -533,7 +541,9 @@ static ra_status check_fwd_ws(const ra_plan* P, int32_t o_is_fp32, const void* w
   if (!workspace) return fail(RA_ERR_INVALID_ARG, "workspace is NULL");
   if (!aligned16(workspace)) return fail(RA_ERR_INVALID_ARG, "workspace must be 16-byte aligned");
   *L = fwd_layout(*P, o_is_fp32);
-  if (bytes < L->total) return fail(RA_ERR_WORKSPACE, "workspace too small: %zu < %zu bytes", bytes, L->total);
+  if (bytes < L->total)
+    return fail(RA_ERR_WORKSPACE, "workspace too small for the ring-step forward: %zu < %zu bytes "
+                "(ra_plan_ring_step_workspace_bytes)", bytes, L->total);
   return RA_OK;
 }
 
@@ -594,8 +604,8 @@ ra_status ra_fwd_finish(const ra_plan* P, void* o, int32_t o_is_fp32, void* work
   return RA_OK;
 }
 
-ra_status ra_fwd(const ra_plan* P, const void* q, const void* k, const void* v, void* o, int32_t o_is_fp32,
-                 float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+ra_status ra_fwd_ring_steps(const ra_plan* P, const void* q, const void* k, const void* v, void* o,
+                            int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
   if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
@@ -633,8 +643,8 @@ ra_status ra_plan_fused_items(const ra_plan* P, int32_t* items, int64_t item_cap
   return RA_OK;
 }
 
-ra_status ra_fwd_fused(const ra_plan* P, const void* q, const void* k, const void* v, void* o, int32_t o_is_fp32,
-                       float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
+ra_status ra_fwd(const ra_plan* P, const void* q, const void* k, const void* v, void* o, int32_t o_is_fp32,
+                 float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
   if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
   if (!q || !k || !v || !o || !lse || !workspace) return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse) || !aligned16(workspace))
@@ -665,8 +675,13 @@ ra_status ra_fwd_fused(const ra_plan* P, const void* q, const void* k, const voi
   p.lse = lse;
   p.status = reinterpret_cast<int*>(ws);
   e = ra::launch_fwd_fused(P->D, tq, tk, tv, p, (int)P->ffw.size(), st);
-  if (e != cudaSuccess) return cuda_fail(e, "fused forward launch");
+  if (e != cudaSuccess) return cuda_fail(e, "forward launch");
   return RA_OK;
+}
+
+ra_status ra_fwd_fused(const ra_plan* P, const void* q, const void* k, const void* v, void* o, int32_t o_is_fp32,
+                       float* lse, void* workspace, size_t workspace_bytes, void* stream) {
+  return ra_fwd(P, q, k, v, o, o_is_fp32, lse, workspace, workspace_bytes, stream);
 }
 
 // ---------------------------------------------------------------- backward

@@ -60,6 +60,14 @@ def load_library(path: str | None = None):
     lib.ra_plan_work_items.restype = i32
     lib.ra_fwd.argtypes = [P, P, P, P, P, i32, P, P, sz, P]
     lib.ra_fwd.restype = i32
+    lib.ra_fwd_ring_steps.argtypes = [P, P, P, P, P, i32, P, P, sz, P]
+    lib.ra_fwd_ring_steps.restype = i32
+    lib.ra_plan_ring_step_workspace_bytes.argtypes = [P, i32, c.POINTER(sz)]
+    lib.ra_plan_ring_step_workspace_bytes.restype = i32
+    lib.ra_fwd_noalloc.argtypes = [P, P, P, P, P, i32, P, P]
+    lib.ra_fwd_noalloc.restype = i32
+    lib.ra_noalloc_status.argtypes = [P]
+    lib.ra_noalloc_status.restype = i32
     lib.ra_bwd.argtypes = [P, P, P, P, P, i32, P, P, P, P, P, i32, P, sz, P]
     lib.ra_bwd.restype = i32
     lib.ra_fwd_prepare.argtypes = [P, i32, P, sz, P]
@@ -156,6 +164,12 @@ class Plan:
         items = [tuple(buf[8 * i:8 * i + 8]) for i in range(n.value)]
         return items, list(off)
 
+    def ring_step_workspace_bytes(self, o_fp32=False):
+        """Workspace bytes of the ring-step forward (one launch per ring step)."""
+        f = ctypes.c_size_t()
+        _check(_lib.ra_plan_ring_step_workspace_bytes(self._handle, int(o_fp32), ctypes.byref(f)))
+        return f.value
+
     def fused_workspace_bytes(self):
         """Workspace bytes of the single-launch forward."""
         f = ctypes.c_size_t()
@@ -199,13 +213,14 @@ def _check_tensor(name, t, shape, dtype):
 
 
 def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, scale=None,
-                  o_fp32=False, plan=None, workspace=None, check=False, fused=False, out=None):
+                  o_fp32=False, plan=None, workspace=None, check=False, fused=None, out=None):
     """Ring attention forward: returns (o [T,Hq,d], lse [Hq,T] fp32).
 
-    ``fused=True`` runs the whole ring in one launch (ra_fwd_fused) instead of
-    one launch per ring step.  ``out=(o, lse)`` writes into caller-owned
-    tensors instead of allocating them.  ``check=True`` synchronises and
-    raises if a kernel reported a timeout.
+    By default (``fused=None`` or ``True``) the whole ring runs in one launch
+    (ra_fwd); ``fused=False`` runs one launch per ring step
+    (ra_fwd_ring_steps).  ``out=(o, lse)`` writes into caller-owned tensors
+    instead of allocating them.  ``check=True`` synchronises and raises if a
+    kernel reported a timeout.
     """
     T, Hq, D = q.shape
     Hkv = k.shape[1]
@@ -223,10 +238,11 @@ def ring_attn_fwd(q, k, v, cu_seqlens, cp_size, layout="zigzag", causal=True, sc
         o, lse = out
         _check_tensor("o", o, (T, Hq, D), ot)
         _check_tensor("lse", lse, (Hq, T), torch.float32)
-    ws_bytes = plan.fused_workspace_bytes() if fused else plan.workspace_bytes(o_fp32=o_fp32)[0]
+    steps = fused is False
+    ws_bytes = plan.ring_step_workspace_bytes(o_fp32) if steps else plan.workspace_bytes(o_fp32=o_fp32)[0]
     if workspace is None or workspace.numel() < ws_bytes:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    call = _lib.ra_fwd_fused if fused else _lib.ra_fwd
+    call = _lib.ra_fwd_ring_steps if steps else _lib.ra_fwd
     _check(call(plan.handle, _ptr(q), _ptr(k), _ptr(v), _ptr(o), int(o_fp32), _ptr(lse),
                 _ptr(workspace), workspace.numel(), _stream(dev)))
     if check:

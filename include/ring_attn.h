@@ -23,7 +23,7 @@
  * On one GPU the ring is run as successive ring steps over key/value shards
  * that already sit in this GPU's memory; there is no communication.
  *
- * Readings where the pages are silent (all documented in the design notes):
+ * Readings taken where the pages are silent:
  *   - combine = exact log-sum-exp merge of normalised partials;
  *   - zigzag layout: 2*cp equal chunks per document (floor boundaries), rank r
  *     holds chunks r and 2*cp-1-r; contiguous layout: cp floor-boundary parts;
@@ -111,11 +111,21 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
 void ra_plan_destroy(ra_plan* plan);
 
 /*
- * Workspace sizes in bytes for ra_fwd (given o_is_fp32) and ra_bwd (given
- * grads_fp32).  Either output pointer may be NULL.
+ * Workspace sizes in bytes for ra_fwd (status header, work list and key-tile
+ * table; the same for either output dtype, o_is_fp32 is accepted for
+ * symmetry) and ra_bwd (given grads_fp32: bf16 gradients add their fp32
+ * accumulators).  Either output pointer may be NULL.
  */
 ra_status ra_plan_workspace_bytes(const ra_plan* plan, int32_t o_is_fp32, int32_t grads_fp32,
                                   size_t* fwd_bytes, size_t* bwd_bytes);
+
+/*
+ * Workspace bytes of the ring-step forward (ra_fwd_ring_steps, and
+ * ra_fwd_prepare / ra_fwd_ring_step / ra_fwd_finish): status header, work
+ * list and, for a bf16 output (o_is_fp32 == 0), the fp32 running output
+ * [T, Hq, d] that the steps merge into.
+ */
+ra_status ra_plan_ring_step_workspace_bytes(const ra_plan* plan, int32_t o_is_fp32, size_t* fwd_bytes);
 
 /*
  * Plan statistics: number of ring steps (max cp over documents), visible
@@ -178,7 +188,8 @@ ra_status ra_dynamic_cp(const int32_t* doc_lengths, int32_t num_docs, int32_t nu
                         int64_t* rank_tokens);
 
 /*
- * Forward in one launch over the whole ring (same result as ra_fwd).  Each
+ * ra_fwd_fused: the same call as ra_fwd (kept under this name).
+ * ra_fwd: the forward in one launch over the whole ring.  Each
  * CTA keeps one 256-row query chunk's running (O, row max, row sums) on chip
  * and visits the key/value shards in ring order, s = 0 .. cp-1 (shard
  * (r - s) mod cp): the merge of step s into the running state is the online
@@ -187,14 +198,23 @@ ra_status ra_dynamic_cp(const int32_t* doc_lengths, int32_t num_docs, int32_t nu
  * incrementally as the KV blocks circulate; Accelerate guide, "Detalhes
  * tecnicos": `combine` of the per-shard results), so no running output goes
  * through HBM between steps and O is written once, in its final dtype.
- * Arguments as ra_fwd; workspace: device, >= ra_plan_fused_workspace_bytes.
- * The caller owns every buffer; errors as ra_fwd (RA_ERR_WORKSPACE when the
- * workspace is too small).
+ * Within a chunk the online softmax visits exactly the key tiles that the
+ * ring steps would, in the same order, so the result equals the ring-step
+ * forward (ra_fwd_ring_steps) up to fp32 rounding.
+ *   q [T,Hq,d] bf16, k/v [T,Hkv,d] bf16 (device).
+ *   o [T,Hq,d]: bf16, or fp32 when o_is_fp32 != 0 (device, written).
+ *   lse [Hq,T] fp32 natural-log log-sum-exp (device, written).
+ *   workspace: device, >= ra_plan_workspace_bytes(..).fwd.
+ * The caller owns every buffer; RA_ERR_WORKSPACE when the workspace is too
+ * small.
  */
+ra_status ra_fwd(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
+                 int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                 void* stream);
 ra_status ra_fwd_fused(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
                        int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes, void* stream);
 
-/* Workspace bytes of ra_fwd_fused (header, work list, key-tile table). */
+/* Workspace bytes of ra_fwd / ra_fwd_fused (header, work list, key-tile table). */
 ra_status ra_plan_fused_workspace_bytes(const ra_plan* plan, size_t* fwd_bytes);
 
 /*
@@ -210,19 +230,16 @@ ra_status ra_plan_fused_items(const ra_plan* plan, int32_t* items, int64_t item_
                               int64_t tile_capacity, int64_t* num_items, int64_t* num_tiles);
 
 /*
- * Forward: for s = 0 .. steps-1 every query shard r attends to key/value
- * shard (r - s) mod cp of its document (one kernel launch per ring step,
- * tcgen05 tensor-core block attention with online softmax); each step's
- * partial (O_s, LSE_s) is merged exactly into the running (O, LSE) in the
- * step kernel's epilogue.
- *   q [T,Hq,d] bf16, k/v [T,Hkv,d] bf16 (device).
- *   o [T,Hq,d]: bf16, or fp32 when o_is_fp32 != 0 (device, written).
- *   lse [Hq,T] fp32 natural-log log-sum-exp (device, written).
- *   workspace: device, >= ra_plan_workspace_bytes(.., o_is_fp32, ..).fwd.
+ * Forward, one launch per ring step: for s = 0 .. steps-1 every query shard r
+ * attends to key/value shard (r - s) mod cp of its document (tcgen05
+ * tensor-core block attention with online softmax); each step's partial
+ * (O_s, LSE_s) is merged exactly into the running (O, LSE) in the step
+ * kernel's epilogue.  Arguments as ra_fwd; workspace: device,
+ * >= ra_plan_ring_step_workspace_bytes(.., o_is_fp32, ..).
  */
-ra_status ra_fwd(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
-                 int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes,
-                 void* stream);
+ra_status ra_fwd_ring_steps(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
+                            int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /*
  * Backward from the saved LSE: Delta = rowsum(dout * o) (o as returned by
@@ -239,9 +256,9 @@ ra_status ra_bwd(const ra_plan* plan, const void* q, const void* k, const void* 
                  size_t workspace_bytes, void* stream);
 
 /*
- * The ring step as its own call.  ra_fwd is exactly
+ * The ring step as its own call.  ra_fwd_ring_steps is exactly
  *   ra_fwd_prepare; ra_fwd_ring_step(s) for s = 0 .. steps-1; ra_fwd_finish
- * and ra_bwd is
+ * (workspace >= ra_plan_ring_step_workspace_bytes) and ra_bwd is
  *   ra_bwd_prepare; ra_bwd_ring_step(s) for every s; ra_bwd_finish
  * on one workspace.  A multi-GPU driver would call the ring step after each
  * key/value exchange (NVSHMEM/XLA page, "Patrones de comunicacion en la
@@ -304,19 +321,29 @@ ra_status ra_workspace_status(const void* workspace, void* stream);
  * Same computation and arguments as ra_fwd, minus the workspace: the
  * workspace is a fixed 32 MiB device array inside this library, held on
  * every GPU that loads it until the process exits.
- *   - A plan whose forward workspace exceeds 32 MiB is rejected with
- *     RA_ERR_WORKSPACE (ra_plan_workspace_bytes gives the need; o_is_fp32 = 1
- *     removes the fp32 running output from it).
+ *   - A plan whose forward workspace (ra_plan_workspace_bytes(..).fwd: the
+ *     work list and key-tile table) exceeds 32 MiB is rejected with
+ *     RA_ERR_WORKSPACE before any GPU work.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress) with that device current, and so does the first
+ *     call after the device's context was re-created (cudaDeviceReset); make
+ *     those first calls before any stream capture.
  *   - All calls share the one array: calls that may overlap on the GPU (other
  *     streams, other host threads) race and must be serialised by the caller.
- *   - A kernel timeout is recorded in the array, which ra_workspace_status
- *     cannot reach; validate outputs if that matters.
+ *     Each call zeroes the array's status word and rewrites its work lists
+ *     before the kernel reads them.
  */
 ra_status ra_fwd_noalloc(const ra_plan* plan, const void* q, const void* k, const void* v, void* o,
                          int32_t o_is_fp32, float* lse, void* stream);
+
+/*
+ * Status of the last ra_fwd_noalloc call on the current device, read from
+ * the fixed array's status word after synchronising `stream` (as
+ * ra_workspace_status does for a caller's workspace): RA_OK, or
+ * RA_ERR_TIMEOUT if its kernel gave up on a pipeline wait (the outputs are
+ * then undefined).  Allocates nothing.
+ */
+ra_status ra_noalloc_status(void* stream);
 
 /* Thread-local text for the last non-OK status returned on this thread. */
 const char* ra_last_error(void);

@@ -148,6 +148,60 @@ def attention_rows(q, k, v, cu_seqlens, rows, head, causal=True, scale=None):
     return o, lse
 
 
+def attention_keys_dkdv(q, k, v, do, cu_seqlens, keys, kv_head, causal=True, scale=None):
+    """dk and dv of single key rows of one key/value head (exact).
+
+    For a key j of document [b, e) the gradients are sums over the queries
+    that see it (i >= j when causal, the whole document otherwise) and over
+    the query heads h of the key/value head's group:
+
+        dv_j = sum_h sum_i P_ij dO_i,   dk_j = scale sum_h sum_i dS_ij q_i,
+        dS_ij = P_ij (<dO_i, v_j> - Delta_i),   Delta_i = <dO_i, O_i>,
+
+    where every P_ij needs the whole softmax row of query i (its LSE and O).
+    So the cost is the number of queries seeing the keys times the document
+    length: cheap for keys near a document's end under a causal mask, which
+    is what the tests at full size ask for.  Returns (dk [len(keys), d],
+    dv [len(keys), d]).
+    """
+    q, k, v, do = _f64(q), _f64(k), _f64(v), _f64(do)
+    T, Hq, d = q.shape
+    G = Hq // k.shape[1]
+    g = kv_head
+    scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+    cu = np.asarray([int(c) for c in cu_seqlens])
+    keys = [int(j) for j in keys]
+    dk = np.zeros((len(keys), d))
+    dv = np.zeros((len(keys), v.shape[2]))
+    # group the keys by document: one pass over the queries that see them
+    by_doc = {}
+    for n, j in enumerate(keys):
+        by_doc.setdefault(int(np.searchsorted(cu, j, side="right") - 1), []).append(n)
+    for doc, idx in by_doc.items():
+        b, e = int(cu[doc]), int(cu[doc + 1])
+        jpos = np.asarray([keys[n] for n in idx])
+        i0 = int(jpos.min()) if causal else b   # first query that sees any of the keys
+        for h in range(g * G, (g + 1) * G):
+            for r0 in range(i0, e, 256):
+                r1 = min(r0 + 256, e)
+                # whole softmax rows of queries [r0, r1): LSE, O and Delta
+                s, kend = _block_scores(q, k, h, g, r0, r1, b, e, causal, scale)
+                lse, p = _softmax_lse(s)
+                o = p @ v[b:kend, g, :]
+                dob = do[r0:r1, h, :]
+                delta = (dob * o).sum(axis=1)
+                # probabilities and dS of these queries against the chosen keys
+                sj = scale * (q[r0:r1, h, :] @ k[jpos, g, :].T)
+                if causal:
+                    sj = np.where(jpos[None, :] <= np.arange(r0, r1)[:, None], sj, -np.inf)
+                pj = np.exp(sj - lse[:, None])
+                dpj = dob @ v[jpos, g, :].T
+                dsj = pj * (dpj - delta[:, None])
+                dv[idx] += pj.T @ dob
+                dk[idx] += scale * (dsj.T @ q[r0:r1, h, :])
+    return dk, dv
+
+
 def attention_rows_dq(q, k, v, do, cu_seqlens, rows, head, causal=True, scale=None):
     """dq of single query rows of one head (exact, O(L d) per row).
 

@@ -360,3 +360,70 @@ def test_pins_catch_a_planted_backward_slip(monkeypatch):
     monkeypatch.setattr(A, "attention_bwd", slipped)
     with pytest.raises(AssertionError):
         test_backward_central_finite_differences()
+
+
+# ---------------------------------------------------------------- gradients of chosen key rows
+
+def _torch_masked_grads(q, k, v, do, cu, causal, scale):
+    """dk, dv through torch float64 autograd of an explicitly masked softmax
+    attention (a mask matrix built from cu_seqlens, GQA by repeating heads)."""
+    T, Hq, d = q.shape
+    G = Hq // k.shape[1]
+    tq = torch.tensor(q)
+    tk = torch.tensor(k, requires_grad=True)
+    tv = torch.tensor(v, requires_grad=True)
+    doc = torch.zeros(T, dtype=torch.long)
+    for n in range(len(cu) - 1):
+        doc[cu[n]:cu[n + 1]] = n
+    pos = torch.arange(T)
+    vis = doc[:, None] == doc[None, :]
+    if causal:
+        vis &= pos[None, :] <= pos[:, None]
+    kk = tk.repeat_interleave(G, dim=1)
+    vv = tv.repeat_interleave(G, dim=1)
+    s = scale * torch.einsum("ihd,jhd->hij", tq, kk)
+    s = s.masked_fill(~vis[None], float("-inf"))
+    o = torch.einsum("hij,jhd->ihd", torch.softmax(s, dim=-1), vv)
+    (o * torch.tensor(do)).sum().backward()
+    return tk.grad.numpy(), tv.grad.numpy()
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_keys_dkdv_matches_torch_autograd(causal):
+    lengths = [37, 1, 300, 22]
+    T, Hq, Hkv, d = sum(lengths), 6, 2, 8
+    q, k, v, do = (_rand((T, Hq, d), 61), _rand((T, Hkv, d), 62),
+                   _rand((T, Hkv, d), 63), _rand((T, Hq, d), 64))
+    cu = _cu(lengths)
+    rk, rv = _torch_masked_grads(q, k, v, do, cu, causal, 0.4)
+    keys = [0, 5, 36, 37, 38, 100, 290, 337, 338, 359]
+    for g in range(Hkv):
+        dk, dv = A.attention_keys_dkdv(q, k, v, do, cu, keys, g, causal=causal, scale=0.4)
+        assert np.abs(dk - rk[keys, g]).max() < 1e-12
+        assert np.abs(dv - rv[keys, g]).max() < 1e-12
+
+
+def test_keys_dkdv_matches_full_oracle():
+    lengths = [600, 45]
+    T, Hq, Hkv, d = sum(lengths), 4, 1, 16
+    q, k, v, do = (_rand((T, Hq, d), 65), _rand((T, Hkv, d), 66),
+                   _rand((T, Hkv, d), 67), _rand((T, Hq, d), 68))
+    cu = _cu(lengths)
+    _, rk, rv, _, _ = A.attention_bwd(q, k, v, do, cu, scale=0.25)
+    keys = list(range(440, 600)) + [600, 644]
+    dk, dv = A.attention_keys_dkdv(q, k, v, do, cu, keys, 0, scale=0.25)
+    assert np.abs(dk - rk[keys, 0]).max() < 1e-12
+    assert np.abs(dv - rv[keys, 0]).max() < 1e-12
+
+
+def test_pins_catch_a_planted_keys_slip(monkeypatch):
+    """An LSE off by a constant (P rows no longer summing to 1) must fail the autograd pin."""
+    orig = A._softmax_lse
+
+    def slipped(s):
+        lse, p = orig(s)
+        return lse + 1e-3, p   # an LSE off by a constant: P no longer sums to 1
+
+    monkeypatch.setattr(A, "_softmax_lse", slipped)
+    with pytest.raises(AssertionError):
+        test_keys_dkdv_matches_torch_autograd(True)

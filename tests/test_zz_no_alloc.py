@@ -3,31 +3,27 @@
 Callers inside a host framework that owns every device allocation, or in a
 loop that must not allocate, get the forward without handing over a
 workspace: the library uses a fixed 32 MiB device array of its own instead.
-These tests call it through the C ABI and compare it with ra_fwd (same
-tolerances as the forward parity tests: 2e-2 on O, 1e-3 on LSE), twice in a
-row with different problems, since every call reuses the same array.
+These tests call it through the C ABI and compare it with ra_fwd on two calls
+in a row with different problems (every call reuses the same array, so a
+stale work list or status word from the previous call would show).  The
+forward has no atomics and ra_fwd_noalloc runs the same kernel as ra_fwd, so
+the outputs must be bit-identical; ra_noalloc_status must read RA_OK.
 
 This file is collected last on purpose.
 """
 
 import ctypes
 
-import numpy as np
 import pytest
 import torch
 
 from workloads import custom, draw_qkvdo
 
-O_TOL, LSE_TOL = 2e-2, 1e-3
-
 
 @pytest.fixture(scope="module")
 def ra():
     import context_ring_attention_step_gb300 as m
-    lib = m.load_library()
-    P = ctypes.c_void_p
-    lib.ra_fwd_noalloc.argtypes = [P, P, P, P, P, ctypes.c_int32, P, P]
-    lib.ra_fwd_noalloc.restype = ctypes.c_int32
+    m.load_library()
     return m
 
 
@@ -37,14 +33,15 @@ def _noalloc(ra, plan, q, k, v, o_fp32):
     o = torch.full((T, Hq, D), float("nan"), dtype=torch.float32 if o_fp32 else torch.bfloat16, device=q.device)
     lse = torch.full((Hq, T), float("nan"), dtype=torch.float32, device=q.device)
     p = ra.ring_attn._ptr
-    st = lib.ra_fwd_noalloc(plan.handle, p(q), p(k), p(v), p(o), int(o_fp32), p(lse), ra.ring_attn._stream(q.device))
+    stream = ra.ring_attn._stream(q.device)
+    st = lib.ra_fwd_noalloc(plan.handle, p(q), p(k), p(v), p(o), int(o_fp32), p(lse), stream)
     assert st == 0, lib.ra_last_error()
-    torch.cuda.synchronize()
-    return o.float().cpu().numpy(), lse.cpu().numpy()
+    assert lib.ra_noalloc_status(stream) == 0, lib.ra_last_error()
+    return o, lse
 
 
 @pytest.mark.gpu
-def test_noalloc_forward_matches_ra_fwd_twice_in_a_row(ra):
+def test_noalloc_forward_equals_ra_fwd_twice_in_a_row(ra):
     if not torch.cuda.is_available():
         pytest.skip("needs a GPU")
     cases = [
@@ -57,18 +54,20 @@ def test_noalloc_forward_matches_ra_fwd_twice_in_a_row(ra):
                        wl.softmax_scale)
         o_ref, lse_ref = ra.ring_attn_fwd(q, k, v, wl.cu_seqlens, list(wl.cp_per_doc), wl.layout, wl.causal,
                                           wl.softmax_scale, o_fp32=o_fp32, plan=plan, check=True)
-        o_ref = o_ref.float().cpu().numpy()
-        lse_ref = lse_ref.cpu().numpy()
         o, lse = _noalloc(ra, plan, q, k, v, o_fp32)
-        assert np.isfinite(o).all() and np.isfinite(lse).all()
-        assert np.abs(o - o_ref).max() <= O_TOL
-        assert np.abs(lse - lse_ref).max() <= LSE_TOL
+        torch.cuda.synchronize()
+        assert torch.isfinite(o.float()).all() and torch.isfinite(lse).all()
+        assert torch.equal(o, o_ref), (wl.name, (o.float() - o_ref.float()).abs().max().item())
+        assert torch.equal(lse, lse_ref), wl.name
 
 
 def test_noalloc_rejects_plans_above_the_scratch_limit(ra):
-    """A plan needing more than 32 MiB of scratch is refused before any GPU work."""
+    """A plan needing more than 32 MiB of scratch is refused before any GPU work.
+
+    512K tokens without a mask, cp 1: 2048 query chunks each meeting 4096 key
+    tiles, 8 bytes per tile in the key-tile table (64 MiB)."""
     lib = ra.load_library()
-    plan = ra.Plan([0, 65536], 8, "zigzag", True, 32, 8, 128)   # bf16 output: 1 GiB running output
+    plan = ra.Plan([0, 524288], 1, "zigzag", False, 1, 1, 64)
     assert plan.workspace_bytes(o_fp32=False)[0] > 32 << 20
     p = ctypes.c_void_p
     st = lib.ra_fwd_noalloc(plan.handle, p(256), p(512), p(768), p(1024), 0, p(1280), p(0))
