@@ -39,6 +39,14 @@ struct ra_plan {
   std::vector<int64_t> fwd_off;  // steps + 1
   std::vector<BwdItem> bwd;
   std::vector<int64_t> bwd_off;  // steps + 1
+  // The same items again, grouped by the query shard that computes them (the
+  // rank of a multi-GPU ring: it keeps its query shard and sees key/value
+  // shard (rank - s) mod cp at step s).  Items of (step s, rank r) are
+  // [off[s * steps + r], off[s * steps + r + 1]).
+  std::vector<FwdItem> fwd_rank;
+  std::vector<int64_t> fwd_rank_off;
+  std::vector<BwdItem> bwd_rank;
+  std::vector<int64_t> bwd_rank_off;
   // single-launch forward over all ring steps: items (kb0 = first tile, ke0 =
   // tile count, kb1/ke1 = active tiles of the two 128-row query tiles) and the
   // key tiles, (start, range end) per tile, ring step by ring step
@@ -52,7 +60,7 @@ struct ra_plan {
   // where pinned memory is unavailable; the calls then copy from the vectors.
   uint8_t* staged = nullptr;
   const uint8_t* staged_dev = nullptr;
-  size_t st_fwd = 0, st_bwd = 0, st_ffw = 0, st_tiles = 0;
+  size_t st_fwd = 0, st_bwd = 0, st_ffw = 0, st_tiles = 0, st_fwdr = 0, st_bwdr = 0;
   ~ra_plan() {
     if (staged) cudaFreeHost(staged);
   }
@@ -102,9 +110,16 @@ void build_items(ra_plan& P) {
   P.bwd.clear();
   P.fwd_off.assign(1, 0);
   P.bwd_off.assign(1, 0);
+  P.fwd_rank.clear();
+  P.bwd_rank.clear();
+  P.fwd_rank_off.assign(1, 0);
+  P.bwd_rank_off.assign(1, 0);
+  auto by_tiles = [](const auto& a, const auto& b) { return a.tiles > b.tiles; };
   for (int32_t s = 0; s < P.steps; ++s) {
     std::vector<FwdItem> fs;
     std::vector<BwdItem> bs;
+    std::vector<std::vector<FwdItem>> fr(P.steps);  // by query shard
+    std::vector<std::vector<BwdItem>> br(P.steps);
     for (int32_t d = 0; d < P.num_docs; ++d) {
       const int32_t base = P.cu[d], L = P.cu[d + 1] - P.cu[d], cp = P.cp[d];
       if (L == 0 || s >= cp) continue;
@@ -133,6 +148,7 @@ void build_items(ra_plan& P) {
             it.flags = s == 0 ? ra::kFirstStep : 0;
             it.tiles = tiles128(it.kb0, it.ke0) + tiles128(it.kb1, it.ke1);
             fs.push_back(it);
+            fr[r].push_back(it);
           }
         }
         // ---- backward: key/value shard r is held by query shard (r + s) mod cp.
@@ -163,16 +179,24 @@ void build_items(ra_plan& P) {
             it.flags = (s == 0 ? ra::kFirstStep : 0) | (g << ra::kHeadShift);
             it.tiles = tiles128(it.qb0, it.qe0) + tiles128(it.qb1, it.qe1);
             bs.push_back(it);
+            br[qr].push_back(it);
           }
         }
       }
     }
     // forward: longest items first, so the tail of each step launch is short
-    std::stable_sort(fs.begin(), fs.end(), [](const FwdItem& a, const FwdItem& b) { return a.tiles > b.tiles; });
+    std::stable_sort(fs.begin(), fs.end(), by_tiles);
     P.fwd.insert(P.fwd.end(), fs.begin(), fs.end());
     P.bwd.insert(P.bwd.end(), bs.begin(), bs.end());
     P.fwd_off.push_back((int64_t)P.fwd.size());
     P.bwd_off.push_back((int64_t)P.bwd.size());
+    for (int32_t r = 0; r < P.steps; ++r) {
+      std::stable_sort(fr[r].begin(), fr[r].end(), by_tiles);
+      P.fwd_rank.insert(P.fwd_rank.end(), fr[r].begin(), fr[r].end());
+      P.bwd_rank.insert(P.bwd_rank.end(), br[r].begin(), br[r].end());
+      P.fwd_rank_off.push_back((int64_t)P.fwd_rank.size());
+      P.bwd_rank_off.push_back((int64_t)P.bwd_rank.size());
+    }
   }
 }
 
@@ -237,13 +261,13 @@ void build_fused(ra_plan& P) {
 int64_t stat_pitch(const ra_plan& P) { return ((int64_t)P.T + 3) & ~int64_t(3); }
 
 struct FwdLayout {
-  size_t items, orun, total;
+  size_t items, ritems, orun, total;
 };
 struct FusedLayout {
   size_t items, tiles, total;
 };
 struct BwdLayout {
-  size_t items, delta, lse2, dq, dk, dv, total;
+  size_t items, ritems, delta, lse2, dq, dk, dv, total;
 };
 
 FwdLayout fwd_layout(const ra_plan& P, int o_fp32) {
@@ -251,6 +275,8 @@ FwdLayout fwd_layout(const ra_plan& P, int o_fp32) {
   size_t off = kHeader;
   l.items = off;
   off = align256(off + P.fwd.size() * sizeof(FwdItem));
+  l.ritems = off;
+  off = align256(off + P.fwd_rank.size() * sizeof(FwdItem));
   l.orun = off;
   if (!o_fp32) off = align256(off + (size_t)P.T * P.Hq * P.D * 4);
   l.total = off;
@@ -273,6 +299,8 @@ BwdLayout bwd_layout(const ra_plan& P, int g_fp32) {
   size_t off = kHeader;
   l.items = off;
   off = align256(off + P.bwd.size() * sizeof(BwdItem));
+  l.ritems = off;
+  off = align256(off + P.bwd_rank.size() * sizeof(BwdItem));
   l.delta = off;
   off = align256(off + (size_t)P.Hq * stat_pitch(P) * 4);
   l.lse2 = off;
@@ -354,7 +382,8 @@ size_t pad16(size_t b) { return (b + 15) & ~size_t(15); }
 void stage_work_lists(ra_plan& P) {
   const size_t bf = pad16(P.fwd.size() * sizeof(FwdItem)), bb = pad16(P.bwd.size() * sizeof(BwdItem));
   const size_t bu = pad16(P.ffw.size() * sizeof(FwdItem)), bt = pad16(P.ftiles.size() * sizeof(int32_t));
-  const size_t total = bf + bb + bu + bt;
+  const size_t bfr = pad16(P.fwd_rank.size() * sizeof(FwdItem)), bbr = pad16(P.bwd_rank.size() * sizeof(BwdItem));
+  const size_t total = bf + bb + bu + bt + bfr + bbr;
   if (total == 0) return;
   const char* off = std::getenv("RA_NO_PINNED_WORK_LISTS");  // tests of the copy fallback
   if (off && off[0] == '1') return;
@@ -375,10 +404,14 @@ void stage_work_lists(ra_plan& P) {
   P.st_bwd = bf;
   P.st_ffw = bf + bb;
   P.st_tiles = bf + bb + bu;
+  P.st_fwdr = bf + bb + bu + bt;
+  P.st_bwdr = bf + bb + bu + bt + bfr;
   if (!P.fwd.empty()) std::memcpy(b + P.st_fwd, P.fwd.data(), P.fwd.size() * sizeof(FwdItem));
   if (!P.bwd.empty()) std::memcpy(b + P.st_bwd, P.bwd.data(), P.bwd.size() * sizeof(BwdItem));
   if (!P.ffw.empty()) std::memcpy(b + P.st_ffw, P.ffw.data(), P.ffw.size() * sizeof(FwdItem));
   if (!P.ftiles.empty()) std::memcpy(b + P.st_tiles, P.ftiles.data(), P.ftiles.size() * sizeof(int32_t));
+  if (!P.fwd_rank.empty()) std::memcpy(b + P.st_fwdr, P.fwd_rank.data(), P.fwd_rank.size() * sizeof(FwdItem));
+  if (!P.bwd_rank.empty()) std::memcpy(b + P.st_bwdr, P.bwd_rank.data(), P.bwd_rank.size() * sizeof(BwdItem));
   P.staged = b;
   P.staged_dev = static_cast<const uint8_t*>(d);
 }
@@ -516,6 +549,23 @@ ra_status ra_plan_work_items(const ra_plan* P, int32_t which, int32_t* items, in
   return RA_OK;
 }
 
+ra_status ra_plan_rank_work_items(const ra_plan* P, int32_t which, int32_t* items, int64_t capacity,
+                                  int64_t* offsets, int64_t* count) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  if (which != 0 && which != 1) return fail(RA_ERR_INVALID_ARG, "which must be 0 (fwd) or 1 (bwd)");
+  const size_t n = which == 0 ? P->fwd_rank.size() : P->bwd_rank.size();
+  if (count) *count = (int64_t)n;
+  if (items) {
+    if (capacity < (int64_t)n) return fail(RA_ERR_INVALID_ARG, "capacity %lld < %zu items", (long long)capacity, n);
+    if (n) std::memcpy(items, which == 0 ? (const void*)P->fwd_rank.data() : (const void*)P->bwd_rank.data(), n * 32);
+  }
+  if (offsets) {
+    const std::vector<int64_t>& off = which == 0 ? P->fwd_rank_off : P->bwd_rank_off;
+    std::copy(off.begin(), off.end(), offsets);
+  }
+  return RA_OK;
+}
+
 ra_status ra_shard_token_ranges(const ra_plan* P, int32_t doc, int32_t rank, int32_t* begin2, int32_t* end2,
                                 int32_t* count) {
   if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
@@ -554,21 +604,20 @@ ra_status ra_fwd_prepare(const ra_plan* P, int32_t o_is_fp32, void* workspace, s
   if (rs != RA_OK) return rs;
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaError_t e = ws_setup(P, ws, st, P->st_fwd, P->fwd.data(), P->fwd.size() * sizeof(FwdItem), L.items);
+  cudaError_t e = ws_setup(P, ws, st, P->st_fwd, P->fwd.data(), P->fwd.size() * sizeof(FwdItem), L.items,
+                           P->st_fwdr, P->fwd_rank.data(), P->fwd_rank.size() * sizeof(FwdItem), L.ritems);
   if (e != cudaSuccess) return cuda_fail(e, "workspace set-up");
   return RA_OK;
 }
 
-ra_status ra_fwd_ring_step(const ra_plan* P, int32_t step, const void* q, const void* k, const void* v, void* o,
-                           int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
-  FwdLayout L;
-  ra_status rs = check_fwd_ws(P, o_is_fp32, workspace, workspace_bytes, &L);
-  if (rs != RA_OK) return rs;
-  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+// One forward ring-step launch over work items [first, first + n) of the list
+// at workspace offset `list` (the per-step list or the per-rank one).
+static ra_status fwd_step_launch(const ra_plan* P, size_t list, int64_t first, int64_t n, const void* q, const void* k,
+                                 const void* v, void* o, int32_t o_is_fp32, float* lse, void* workspace,
+                                 const FwdLayout& L, void* stream_) {
   if (!q || !k || !v || !o || !lse) return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
     return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
-  const int64_t n = P->fwd_off[step + 1] - P->fwd_off[step];
   if (n == 0) return RA_OK;
   CUtensorMap tq, tk, tv;
   if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
@@ -576,7 +625,7 @@ ra_status ra_fwd_ring_step(const ra_plan* P, int32_t step, const void* q, const 
     return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   ra::FwdParams p{};
-  p.items = reinterpret_cast<const FwdItem*>(ws + L.items) + P->fwd_off[step];
+  p.items = reinterpret_cast<const FwdItem*>(ws + list) + first;
   p.Hq = P->Hq;
   p.Hkv = P->Hkv;
   p.T = P->T;
@@ -588,6 +637,29 @@ ra_status ra_fwd_ring_step(const ra_plan* P, int32_t step, const void* q, const 
   cudaError_t e = ra::launch_fwd_step(P->D, tq, tk, tv, p, (int)n, reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return cuda_fail(e, "forward step launch");
   return RA_OK;
+}
+
+ra_status ra_fwd_ring_step(const ra_plan* P, int32_t step, const void* q, const void* k, const void* v, void* o,
+                           int32_t o_is_fp32, float* lse, void* workspace, size_t workspace_bytes, void* stream_) {
+  FwdLayout L;
+  ra_status rs = check_fwd_ws(P, o_is_fp32, workspace, workspace_bytes, &L);
+  if (rs != RA_OK) return rs;
+  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+  return fwd_step_launch(P, L.items, P->fwd_off[step], P->fwd_off[step + 1] - P->fwd_off[step], q, k, v, o,
+                         o_is_fp32, lse, workspace, L, stream_);
+}
+
+ra_status ra_fwd_ring_step_rank(const ra_plan* P, int32_t step, int32_t rank, const void* q, const void* k,
+                                const void* v, void* o, int32_t o_is_fp32, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream_) {
+  FwdLayout L;
+  ra_status rs = check_fwd_ws(P, o_is_fp32, workspace, workspace_bytes, &L);
+  if (rs != RA_OK) return rs;
+  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+  if (rank < 0 || rank >= P->steps) return fail(RA_ERR_INVALID_ARG, "rank %d outside [0, %d)", rank, P->steps);
+  const int64_t c = (int64_t)step * P->steps + rank;
+  return fwd_step_launch(P, L.ritems, P->fwd_rank_off[c], P->fwd_rank_off[c + 1] - P->fwd_rank_off[c], q, k, v, o,
+                         o_is_fp32, lse, workspace, L, stream_);
 }
 
 ra_status ra_fwd_finish(const ra_plan* P, void* o, int32_t o_is_fp32, void* workspace, size_t workspace_bytes,
@@ -728,7 +800,8 @@ ra_status ra_bwd_prepare(const ra_plan* P, const void* o, int32_t o_is_fp32, con
     return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
-  cudaError_t e = ws_setup(P, ws, st, P->st_bwd, P->bwd.data(), P->bwd.size() * sizeof(BwdItem), L.items);
+  cudaError_t e = ws_setup(P, ws, st, P->st_bwd, P->bwd.data(), P->bwd.size() * sizeof(BwdItem), L.items,
+                           P->st_bwdr, P->bwd_rank.data(), P->bwd_rank.size() * sizeof(BwdItem), L.ritems);
   if (e != cudaSuccess) return cuda_fail(e, "workspace set-up");
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
   // the row padding past T is read by the tile loads (and masked): keep it finite
@@ -745,23 +818,20 @@ ra_status ra_bwd_prepare(const ra_plan* P, const void* o, int32_t o_is_fp32, con
   return RA_OK;
 }
 
-ra_status ra_bwd_ring_step(const ra_plan* P, int32_t step, const void* q, const void* k, const void* v,
-                           const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32, void* workspace,
-                           size_t workspace_bytes, void* stream_) {
-  BwdLayout L;
-  ra_status rs = check_bwd_ws(P, grads_fp32, workspace, workspace_bytes, &L);
-  if (rs != RA_OK) return rs;
-  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+// One backward ring-step launch over work items [first, first + n) of the
+// list at workspace offset `list`.
+static ra_status bwd_step_launch(const ra_plan* P, size_t list, int64_t first, int64_t n, const void* q, const void* k,
+                                 const void* v, const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                                 void* workspace, const BwdLayout& L, void* stream_) {
   if (!q || !k || !v || !dout || (grads_fp32 && (!dq || !dk || !dv)))
     return fail(RA_ERR_INVALID_ARG, "NULL tensor pointer");
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(dout) ||
       (grads_fp32 && (!aligned16(dq) || !aligned16(dk) || !aligned16(dv))))
     return fail(RA_ERR_INVALID_ARG, "device pointers must be 16-byte aligned");
-  const int64_t n = P->bwd_off[step + 1] - P->bwd_off[step];
   if (n == 0) return RA_OK;
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
-  p.items = reinterpret_cast<const BwdItem*>(ws + L.items) + P->bwd_off[step];
+  p.items = reinterpret_cast<const BwdItem*>(ws + list) + first;
   CUtensorMap tq, tk, tv, tdo, tl, td, tdq;
   if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
       !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D) ||
@@ -772,6 +842,30 @@ ra_status ra_bwd_ring_step(const ra_plan* P, int32_t step, const void* q, const 
                                       reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return cuda_fail(e, "backward step launch");
   return RA_OK;
+}
+
+ra_status ra_bwd_ring_step(const ra_plan* P, int32_t step, const void* q, const void* k, const void* v,
+                           const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32, void* workspace,
+                           size_t workspace_bytes, void* stream_) {
+  BwdLayout L;
+  ra_status rs = check_bwd_ws(P, grads_fp32, workspace, workspace_bytes, &L);
+  if (rs != RA_OK) return rs;
+  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+  return bwd_step_launch(P, L.items, P->bwd_off[step], P->bwd_off[step + 1] - P->bwd_off[step], q, k, v, dout, dq,
+                         dk, dv, grads_fp32, workspace, L, stream_);
+}
+
+ra_status ra_bwd_ring_step_rank(const ra_plan* P, int32_t step, int32_t rank, const void* q, const void* k,
+                                const void* v, const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                                void* workspace, size_t workspace_bytes, void* stream_) {
+  BwdLayout L;
+  ra_status rs = check_bwd_ws(P, grads_fp32, workspace, workspace_bytes, &L);
+  if (rs != RA_OK) return rs;
+  if (step < 0 || step >= P->steps) return fail(RA_ERR_INVALID_ARG, "step %d outside [0, %d)", step, P->steps);
+  if (rank < 0 || rank >= P->steps) return fail(RA_ERR_INVALID_ARG, "rank %d outside [0, %d)", rank, P->steps);
+  const int64_t c = (int64_t)step * P->steps + rank;
+  return bwd_step_launch(P, L.ritems, P->bwd_rank_off[c], P->bwd_rank_off[c + 1] - P->bwd_rank_off[c], q, k, v, dout,
+                         dq, dk, dv, grads_fp32, workspace, L, stream_);
 }
 
 ra_status ra_bwd_finish(const ra_plan* P, void* dq, void* dk, void* dv, int32_t grads_fp32, void* workspace,

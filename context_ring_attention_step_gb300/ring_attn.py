@@ -79,6 +79,12 @@ def load_library(path: str | None = None):
     for name in ("ra_fwd_prepare", "ra_fwd_ring_step", "ra_fwd_finish", "ra_bwd_prepare", "ra_bwd_ring_step",
                  "ra_bwd_finish"):
         getattr(lib, name).restype = i32
+    lib.ra_fwd_ring_step_rank.argtypes = [P, i32, i32, P, P, P, P, i32, P, P, sz, P]
+    lib.ra_fwd_ring_step_rank.restype = i32
+    lib.ra_bwd_ring_step_rank.argtypes = [P, i32, i32, P, P, P, P, P, P, P, i32, P, sz, P]
+    lib.ra_bwd_ring_step_rank.restype = i32
+    lib.ra_plan_rank_work_items.argtypes = [P, i32, c.POINTER(i32), i64, c.POINTER(i64), c.POINTER(i64)]
+    lib.ra_plan_rank_work_items.restype = i32
     lib.ra_fwd_fused.argtypes = [P, P, P, P, P, i32, P, P, sz, P]
     lib.ra_fwd_fused.restype = i32
     lib.ra_plan_fused_workspace_bytes.argtypes = [P, c.POINTER(sz)]
@@ -120,6 +126,7 @@ class Plan:
             per_doc = _i32_array(cp_size)
         else:
             cp_all = int(cp_size)
+        self.cp_per_doc = [int(x) for x in cp_size] if per_doc is not None else [cp_all] * self.num_docs
         self._handle = ctypes.c_void_p()
         self.layout = layout
         self.causal = bool(causal)
@@ -169,6 +176,22 @@ class Plan:
         f = ctypes.c_size_t()
         _check(_lib.ra_plan_ring_step_workspace_bytes(self._handle, int(o_fp32), ctypes.byref(f)))
         return f.value
+
+    def rank_work_items(self, which="fwd"):
+        """Per-rank work lists: {(step, rank): [items as 8-int tuples]}."""
+        w = 0 if which == "fwd" else 1
+        n = ctypes.c_int64()
+        _check(_lib.ra_plan_rank_work_items(self._handle, w, None, 0, None, ctypes.byref(n)))
+        steps = self.stats()["steps"]
+        buf = (ctypes.c_int32 * max(1, 8 * n.value))()
+        off = (ctypes.c_int64 * (steps * steps + 1))()
+        _check(_lib.ra_plan_rank_work_items(self._handle, w, buf, n.value, off, ctypes.byref(n)))
+        out = {}
+        for s in range(steps):
+            for r in range(steps):
+                c = s * steps + r
+                out[(s, r)] = [tuple(buf[8 * i:8 * i + 8]) for i in range(off[c], off[c + 1])]
+        return out
 
     def fused_workspace_bytes(self):
         """Workspace bytes of the single-launch forward."""

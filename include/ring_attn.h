@@ -295,6 +295,39 @@ ra_status ra_bwd_finish(const ra_plan* plan, void* dq, void* dk, void* dv, int32
                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * The ring step of one rank, for a multi-GPU ring (one process per GPU, rank
+ * r keeps query shard r and holds key/value shard (r - s) mod cp at step s:
+ * NVSHMEM/XLA page, "Patrones de comunicacion en la atencion en anillo";
+ * Accelerate guide, "Detalhes tecnicos").  Same as ra_fwd_ring_step /
+ * ra_bwd_ring_step, restricted to the work items of query shard `rank`
+ * (rank in [0, steps)): the kernel reads only key/value rows of shard
+ * (rank - step) mod cp and writes only the running output rows of shard rank
+ * (forward), or dQ rows of shard rank and dK/dV rows of shard
+ * (rank - step) mod cp (backward).  Tensors keep the global THD layout
+ * [T, H, d]: a rank's buffers are full length and only the rows of the shards
+ * it holds are used; every other row of q, k, v, o, dout and of the running
+ * output must hold finite values (zeros), since 128-row tiles overhang a
+ * shard's ranges and a masked probability of 0 times a NaN is not 0.
+ * Workspaces and prepare/finish calls as for the all-ranks calls
+ * (ra_fwd_prepare puts both work lists in place).
+ */
+ra_status ra_fwd_ring_step_rank(const ra_plan* plan, int32_t step, int32_t rank, const void* q, const void* k,
+                                const void* v, void* o, int32_t o_is_fp32, float* lse, void* workspace,
+                                size_t workspace_bytes, void* stream);
+ra_status ra_bwd_ring_step_rank(const ra_plan* plan, int32_t step, int32_t rank, const void* q, const void* k,
+                                const void* v, const void* dout, void* dq, void* dk, void* dv, int32_t grads_fp32,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * The per-rank work lists, for inspection and tests: items as in
+ * ra_plan_work_items, grouped by (step, rank); offsets: host
+ * int64[steps * steps + 1] or NULL (items of step s, rank r are
+ * [off[s * steps + r], off[s * steps + r + 1])).
+ */
+ra_status ra_plan_rank_work_items(const ra_plan* plan, int32_t which, int32_t* items, int64_t capacity,
+                                  int64_t* offsets, int64_t* count);
+
+/*
  * Failure-detection self-test (no counterpart on the pages): enqueue one small
  * kernel that waits, through the same bounded mbarrier wait the ring kernels
  * use, on a barrier that nothing ever arrives on.  After limit_us microseconds

@@ -267,3 +267,42 @@ def test_missing_library_fails_loudly(tmp_path):
             m.load_library(str(tmp_path / "absent.so"))
     finally:
         m._lib = saved
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("lengths,cp", [([512], 4), ([700, 3, 1, 260], [4, 2, 1, 3]), ([1000], 1)])
+def test_rank_work_lists_partition_each_step(ra, layout, lengths, cp):
+    """The per-rank lists of a step hold exactly the step's items, and rank r's
+    items are those of query shard r (forward: query rows in shard r;
+    backward: key rows in shard (r - s) mod cp, queries in shard r)."""
+    cu = [0]
+    for L in lengths:
+        cu.append(cu[-1] + L)
+    plan = ra.Plan(cu, cp, layout, True, 4, 2, 64)
+    cps = plan.cp_per_doc
+    steps = plan.stats()["steps"]
+
+    def shard_rows(r):
+        rows = set()
+        for d in range(len(lengths)):
+            if r < cps[d]:
+                for b, e in plan.shard_token_ranges(d, r):
+                    rows.update(range(b, e))
+        return rows
+
+    for which in ("fwd", "bwd"):
+        items, off = plan.work_items(which)
+        per_rank = plan.rank_work_items(which)
+        for s in range(steps):
+            got = sorted(it for r in range(steps) for it in per_rank[(s, r)])
+            assert got == sorted(items[off[s]:off[s + 1]])
+            for r in range(steps):
+                rows_r = shard_rows(r)
+                for it in per_rank[(s, r)]:
+                    if which == "fwd":
+                        assert set(range(it[0], it[1])) <= rows_r
+                    else:
+                        qs = set(range(it[2], it[3])) | set(range(it[4], it[5]))
+                        assert qs <= rows_r
+                        d = next(i for i in range(len(lengths)) if cu[i] <= it[0] < cu[i + 1])
+                        assert set(range(it[0], it[1])) <= shard_rows((r - s) % cps[d]) or cps[d] <= s
