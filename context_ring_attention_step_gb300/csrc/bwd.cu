@@ -82,8 +82,6 @@ __device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float 
                : "memory");
 }
 
-__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
 template <int D>
 __global__ void __launch_bounds__(512, 1)
@@ -343,7 +341,11 @@ __global__ void __launch_bounds__(512, 1)
       cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
       cmax = qe - q0;  // exclusive
     };
-    uint32_t pk[32];  // P^T of the current pair, bf16 pairs (kept for its dS phase)
+    // P^T of the current pair in fp32 (masked), kept for its dS phase: dS is
+    // formed from the unrounded P, so it carries one bf16 rounding (its own,
+    // for the dK/dQ MMAs) instead of two; only the dV MMA consumes the
+    // bf16-rounded P.
+    float pf[64];
     // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64),
     // packed into this warpgroup's own columns of the S region (never into the
     // other warpgroup's columns, which it may not have read yet)
@@ -373,12 +375,16 @@ __global__ void __launch_bounds__(512, 1)
             if (c0 < cmin || c0 >= cmax) p0 = 0.f;
             if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
           }
-          pk[16 * c + x] = pack_bf16x2(p0, p1);
+          pf[32 * c + 2 * x] = p0;
+          pf[32 * c + 2 * x + 1] = p1;
         }
       }
       uint32_t w0[16], w1[16];
 #pragma unroll
-      for (int x = 0; x < 16; ++x) { w0[x] = pk[x]; w1[x] = pk[16 + x]; }
+      for (int x = 0; x < 16; ++x) {
+        w0[x] = pack_bf16x2(pf[2 * x], pf[2 * x + 1]);
+        w1[x] = pack_bf16x2(pf[32 + 2 * x], pf[32 + 2 * x + 1]);
+      }
       tmem_st16(tS + 64 * wg, w0);
       tmem_st16(tS + 64 * wg + 16, w1);
       tmem_st_wait();
@@ -406,11 +412,10 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 64 * wg + 32 * c + 2 * x;
-          const uint32_t pp = pk[16 * c + x];
           const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
           const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
-          const float d0 = bf16lo(pp) * (__uint_as_float(r[c][2 * x]) - da) * scale;
-          const float d1 = bf16hi(pp) * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
+          const float d0 = pf[32 * c + 2 * x] * (__uint_as_float(r[c][2 * x]) - da) * scale;
+          const float d1 = pf[32 * c + 2 * x + 1] * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
           w[c][x] = pack_bf16x2(d0, d1);
         }
       }

@@ -106,12 +106,14 @@ def test_varlen_65k_full_kv_group(ra):
     _full_group_check(ra, workload("varlen_65k"))
 
 
-@pytest.mark.parametrize("d,causal", [(128, True), (128, False), (64, True)])
-def test_dkdv_chain_flush_cp1(ra, d, causal):
-    """cp = 1 over a 8000-token document: the first key tiles meet 63 query
-    tiles x 12 heads = 756 pairs, i.e. two chain flushes mid-CTA (at pairs 256
-    and 512, inside query heads 4 and 8) before the final one."""
-    wl = custom([8000, 1500], 12, 1, d, [1, 1], "zigzag", causal, seed=51, name="chain_flush")
+@pytest.mark.parametrize("d,causal,L", [(128, True, 24000), (128, False, 9000), (64, True, 24000)])
+def test_dkdv_chain_flush_cp1(ra, d, causal, L):
+    """cp = 1, 4 query heads on one kv head (the GQA ratio of the workloads):
+    the first key tiles of a 24000-token causal document meet 188 query tiles
+    x 4 heads = 752 pairs, i.e. two chain flushes mid-CTA (at pairs 256 and
+    512, inside query heads 1 and 2) before the final one; without a mask a
+    9000-token document gives 71 x 4 = 284 pairs, one flush."""
+    wl = custom([L, 1500], 4, 1, d, [1, 1], "zigzag", causal, seed=51, name="chain_flush")
     q, k, v, do = draw_qkvdo(wl)
     ref = _group_reference(wl, q, k, v, do, 0)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
