@@ -105,6 +105,10 @@ int shard(int32_t L, int32_t cp, int32_t layout, int32_t r, int32_t* b, int32_t*
 
 int32_t tiles128(int32_t a, int32_t b) { return b > a ? (b - a + 127) / 128 : 0; }
 
+// Query rows of one forward CTA: two 128-row tiles at head_dim 64/128, one at
+// head_dim 256 (whose output accumulator alone takes half of tensor memory).
+int32_t rows_per_item(const ra_plan& P) { return P.D == 256 ? 128 : 256; }
+
 void build_items(ra_plan& P) {
   P.fwd.clear();
   P.bwd.clear();
@@ -130,8 +134,8 @@ void build_items(ra_plan& P) {
         const int nq = shard(L, cp, P.layout, r, qb, qe);
         const int nk = shard(L, cp, P.layout, j, kb, ke);
         for (int a = 0; a < nq; ++a) {
-          for (int32_t q0 = base + qb[a]; q0 < base + qe[a]; q0 += 256) {
-            const int32_t q1 = std::min(q0 + 256, base + qe[a]);
+          for (int32_t q0 = base + qb[a]; q0 < base + qe[a]; q0 += rows_per_item(P)) {
+            const int32_t q1 = std::min(q0 + rows_per_item(P), base + qe[a]);
             FwdItem it{};
             it.q0 = q0;
             it.q1 = q1;
@@ -216,8 +220,8 @@ void build_fused(ra_plan& P) {
       int32_t qb[2], qe[2];
       const int nq = shard(L, cp, P.layout, r, qb, qe);
       for (int a = 0; a < nq; ++a) {
-        for (int32_t q0 = base + qb[a]; q0 < base + qe[a]; q0 += 256) {
-          const int32_t q1 = std::min(q0 + 256, base + qe[a]);
+        for (int32_t q0 = base + qb[a]; q0 < base + qe[a]; q0 += rows_per_item(P)) {
+          const int32_t q1 = std::min(q0 + rows_per_item(P), base + qe[a]);
           const int32_t last0 = std::min(q0 + 128, q1) - 1, last1 = q1 - 1;
           const bool two = q0 + 128 < q1;
           FwdItem it{};
@@ -333,26 +337,27 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// THD bf16 tensor [T, H, D] as a 3-D map {D, H, T}; box {64, 1, 128}, 128-byte swizzle.
-bool encode_thd(CUtensorMap* m, const void* base, int T, int H, int D) {
+// THD bf16 tensor [T, H, D] as a 3-D map {D, H, T}; box {64, 1, rows} (rows = 128,
+// or 64 for the head_dim 256 backward's query tiles), 128-byte swizzle.
+bool encode_thd(CUtensorMap* m, const void* base, int T, int H, int D, int rows = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
   cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
-  cuuint32_t box[3] = {64, 1, 128};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)rows};
   cuuint32_t estr[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Per-head fp32 rows [Hq, pitch] as a 2-D map {pitch, Hq}; box {128, 1}.
-bool encode_rows(CUtensorMap* m, const void* base, int64_t pitch, int H) {
+// Per-head fp32 rows [Hq, pitch] as a 2-D map {pitch, Hq}; box {width, 1}.
+bool encode_rows(CUtensorMap* m, const void* base, int64_t pitch, int H, int width = 128) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {(cuuint64_t)pitch, (cuuint64_t)H};
   cuuint64_t strides[1] = {(cuuint64_t)pitch * 4};
-  cuuint32_t box[2] = {128, 1};
+  cuuint32_t box[2] = {(cuuint32_t)width, 1};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
@@ -461,8 +466,8 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
   if (num_q_heads < 1 || num_kv_heads < 1 || num_q_heads % num_kv_heads != 0)
     return fail(RA_ERR_INVALID_ARG, "need Hq >= 1, Hkv >= 1 and Hq %% Hkv == 0 (got %d, %d)", num_q_heads,
                 num_kv_heads);
-  if (head_dim != 64 && head_dim != 128)
-    return fail(RA_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", head_dim);
+  if (head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(RA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256 (got %d)", head_dim);
   if (!(softmax_scale == softmax_scale) || std::isinf(softmax_scale))
     return fail(RA_ERR_INVALID_ARG, "softmax_scale must be finite");
   if (cu_seqlens[0] != 0) return fail(RA_ERR_INVALID_ARG, "cu_seqlens[0] must be 0");
@@ -832,14 +837,19 @@ static ra_status bwd_step_launch(const ra_plan* P, size_t list, int64_t first, i
   uint8_t* ws = reinterpret_cast<uint8_t*>(workspace);
   ra::BwdParams p = bwd_params(P, L, ws, dq, dk, dv, grads_fp32);
   p.items = reinterpret_cast<const BwdItem*>(ws + list) + first;
+  // head_dim 256: 64-row query tiles (with K and V resident, shared memory
+  // holds one 64-row Q and dO tile)
+  const int qrows = P->D == 256 ? 64 : 128;
   CUtensorMap tq, tk, tv, tdo, tl, td, tdq;
-  if (!encode_thd(&tq, q, P->T, P->Hq, P->D) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
-      !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D) ||
-      !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq) || !encode_rows(&td, p.delta, p.stat_pitch, P->Hq) ||
-      !encode_acc(&tdq, p.dq_acc, P->T, P->Hq, P->D))
+  if (!encode_thd(&tq, q, P->T, P->Hq, P->D, qrows) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
+      !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D, qrows) ||
+      !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq, qrows) ||
+      !encode_rows(&td, p.delta, p.stat_pitch, P->Hq, qrows) || !encode_acc(&tdq, p.dq_acc, P->T, P->Hq, P->D))
     return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
-  cudaError_t e = ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
-                                      reinterpret_cast<cudaStream_t>(stream_));
+  cudaError_t e = P->D == 256 ? ra::launch_bwd_step_d256(tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
+                                                          reinterpret_cast<cudaStream_t>(stream_))
+                              : ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
+                                                    reinterpret_cast<cudaStream_t>(stream_));
   if (e != cudaSuccess) return cuda_fail(e, "backward step launch");
   return RA_OK;
 }

@@ -147,6 +147,8 @@ cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout
     bwd_preprocess_kernel<128><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
   else if (D == 64)
     bwd_preprocess_kernel<64><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
+  else if (D == 256)
+    bwd_preprocess_kernel<256><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

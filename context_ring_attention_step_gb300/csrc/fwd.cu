@@ -674,6 +674,7 @@ cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorM
                             const FwdParams& p, int num_items, cudaStream_t stream) {
   if (head_dim == 128) return launch<128, false>(tq, tk, tv, p, num_items, stream);
   if (head_dim == 64) return launch<64, false>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 256) return launch_fwd_step_d256(tq, tk, tv, p, num_items, stream);
   return cudaErrorInvalidValue;
 }
 
@@ -681,6 +682,7 @@ cudaError_t launch_fwd_fused(int head_dim, const CUtensorMap& tq, const CUtensor
                              const FwdParams& p, int num_items, cudaStream_t stream) {
   if (head_dim == 128) return launch<128, true>(tq, tk, tv, p, num_items, stream);
   if (head_dim == 64) return launch<64, true>(tq, tk, tv, p, num_items, stream);
+  if (head_dim == 256) return launch_fwd_fused_d256(tq, tk, tv, p, num_items, stream);
   return cudaErrorInvalidValue;
 }
 

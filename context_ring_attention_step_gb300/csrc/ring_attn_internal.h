@@ -10,8 +10,8 @@
 
 namespace ra {
 
-// Forward work item: one CTA = up to 256 query rows (two 128-row tiles) of one
-// query chunk, all in one document, against up to two key ranges of the
+// Forward work item: one CTA = up to 256 query rows (two 128-row tiles; one
+// tile at head_dim 256) of one query chunk, all in one document, against up to two key ranges of the
 // key/value shard that the query shard holds at this ring step.  Ranges are
 // global token positions, sorted, disjoint, already clipped to the keys the
 // rows may see (for causal: keys < q1).  Grid: items x Hq.
@@ -78,10 +78,19 @@ cudaError_t launch_fwd_fused(int head_dim, const CUtensorMap& tq, const CUtensor
 cudaError_t launch_fwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const FwdParams& p, int num_items,
                             cudaStream_t stream);
+// head_dim 256 (fwd256.cu): one 128-row query tile per CTA
+cudaError_t launch_fwd_step_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const FwdParams& p, int num_items, cudaStream_t stream);
+cudaError_t launch_fwd_fused_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                  const FwdParams& p, int num_items, cudaStream_t stream);
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tlse2,
                             const CUtensorMap& tdelta, const CUtensorMap& tdq_acc, const BwdParams& p,
                             int num_items, cudaStream_t stream);
+// head_dim 256 (bwd256.cu): two CTAs per work item (column halves), 64-row query tiles
+cudaError_t launch_bwd_step_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
+                                 const CUtensorMap& tdo, const CUtensorMap& tl, const CUtensorMap& td,
+                                 const CUtensorMap& tdq, const BwdParams& p, int num_items, cudaStream_t stream);
 // o (bf16) = o_run (fp32), elementwise.
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, int site, cudaStream_t stream);

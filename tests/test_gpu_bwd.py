@@ -65,9 +65,17 @@ def test_multi_tile_ragged_gqa(ra, layout, causal):
     _check_vs_oracle(ra, wl)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_varlen_docs_per_doc_cp(ra, d):
     wl = custom([300, 1, 5, 777, 129, 64], 4, 1, d, [3, 1, 2, 5, 8, 1], "zigzag", True, seed=22, name="varlen")
+    _check_vs_oracle(ra, wl)
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_256_ragged_gqa(ra, layout, causal):
+    """head_dim 256: two CTAs per key tile (column halves), 64-row query tiles."""
+    wl = custom([1500, 77], 4, 2, 256, [3, 2], layout, causal, seed=25, name="d256_bwd")
     _check_vs_oracle(ra, wl)
 
 

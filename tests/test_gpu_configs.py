@@ -213,6 +213,10 @@ def test_head_dim_64_at_128k(ra):
     _check(ra, workload("long_128k_d64"), heads=(2, 30), nrows=12)
 
 
+def test_head_dim_256_at_128k(ra):
+    _check(ra, workload("long_128k_d256"), heads=(1, 14), nrows=12)
+
+
 def test_varlen_65k_with_dynamic_cp_sizes(ra):
     """The varlen batch with per-document cp chosen by ra_dynamic_cp (8 ranks,
     12288 tokens per rank): same parity bar on sampled rows and identities."""

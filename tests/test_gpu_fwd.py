@@ -62,10 +62,32 @@ def test_multi_tile_ragged_gqa(ra, layout, causal):
     _check_vs_oracle(ra, wl)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_varlen_docs_per_doc_cp(ra, d):
     wl = custom([300, 1, 5, 777, 129, 64], 4, 1, d, [3, 1, 2, 5, 8, 1], "zigzag", True, seed=12, name="varlen")
     _check_vs_oracle(ra, wl)
+
+
+# ---- head_dim 256: one 128-row query tile per CTA, S double-buffered
+
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_head_dim_256_ragged_gqa(ra, fused, layout, causal):
+    wl = custom([1500, 77], 4, 2, 256, [3, 2], layout, causal, seed=15, name="d256")
+    _check_vs_oracle(ra, wl, fused=fused)
+
+
+def test_head_dim_256_ring_equals_cp1_fp32(ra):
+    wl = custom([2048, 700], 4, 2, 256, 4, "zigzag", True, seed=16, name="d256_ring_vs_cp1")
+    q, k, v, _ = draw_qkvdo(wl)
+    o1, l1 = _run_fwd(ra, wl, q, k, v, o_fp32=True, cp=[1, 1])
+    for layout in ("zigzag", "contiguous"):
+        for cp in ([4, 4], [8, 3]):
+            for fused in (False, True):
+                o, l = _run_fwd(ra, wl, q, k, v, o_fp32=True, cp=cp, layout=layout, fused=fused)
+                assert np.abs(o - o1).max() <= RING_TOL, (layout, cp, fused, np.abs(o - o1).max())
+                assert np.abs(l - l1).max() <= RING_TOL
 
 
 def test_ring_equals_gpu_cp1_fp32(ra):
@@ -115,7 +137,7 @@ def test_fused_multi_tile_ragged_gqa(ra, layout, causal):
     _check_vs_oracle(ra, wl, fused=True)
 
 
-@pytest.mark.parametrize("d", [64, 128])
+@pytest.mark.parametrize("d", [64, 128, 256])
 def test_fused_varlen_docs_per_doc_cp(ra, d):
     wl = custom([300, 1, 5, 777, 129, 64], 4, 1, d, [3, 1, 2, 5, 8, 1], "zigzag", True, seed=12, name="varlen")
     _check_vs_oracle(ra, wl, fused=True)

@@ -106,13 +106,15 @@ def test_varlen_65k_full_kv_group(ra):
     _full_group_check(ra, workload("varlen_65k"))
 
 
-@pytest.mark.parametrize("d,causal,L", [(128, True, 24000), (128, False, 9000), (64, True, 24000)])
+@pytest.mark.parametrize("d,causal,L", [(128, True, 24000), (128, False, 9000), (64, True, 24000),
+                                         (256, True, 9000)])
 def test_dkdv_chain_flush_cp1(ra, d, causal, L):
     """cp = 1, 4 query heads on one kv head (the GQA ratio of the workloads):
     the first key tiles of a 24000-token causal document meet 188 query tiles
     x 4 heads = 752 pairs, i.e. two chain flushes mid-CTA (at pairs 256 and
     512, inside query heads 1 and 2) before the final one; without a mask a
-    9000-token document gives 71 x 4 = 284 pairs, one flush."""
+    9000-token document gives 71 x 4 = 284 pairs, one flush.  At head_dim 256
+    the query tiles are 64 rows: 141 x 4 = 564 pairs, two flushes."""
     wl = custom([L, 1500], 4, 1, d, [1, 1], "zigzag", causal, seed=51, name="chain_flush")
     q, k, v, do = draw_qkvdo(wl)
     ref = _group_reference(wl, q, k, v, do, 0)

@@ -101,10 +101,12 @@ CONFIGS = {
     "long_128k": _single("long_128k", 131072, 32, 8, 128, 16, "zigzag", 3),
     "varlen_65k": _varlen(),
     "max_256k": _single("max_256k", 262144, 32, 8, 128, 32, "zigzag", 5),
-    # beyond the five parity configurations: the no-mask mode and head_dim 64 at 128K
+    # beyond the five parity configurations: the no-mask mode and head_dim 64 / 256 at 128K
     "long_128k_noncausal": Workload("long_128k_noncausal", 131072, 32, 8, 128, (0, 131072), (16,), "zigzag",
                                     False, 6),
     "long_128k_d64": _single("long_128k_d64", 131072, 32, 8, 64, 16, "zigzag", 7),
+    # head_dim 256 at 128K (16 query / 8 key-value heads: the same useful FLOPs as 32 heads at 128)
+    "long_128k_d256": _single("long_128k_d256", 131072, 16, 8, 256, 16, "zigzag", 8),
 }
 
 
