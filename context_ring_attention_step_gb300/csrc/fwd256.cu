@@ -89,7 +89,11 @@ __global__ void __launch_bounds__(256, 1)
   const uint32_t b_p = smem_u32(bars + 3 + 2 * kStages);      // P(j) written
   const uint32_t b_o = smem_u32(bars + 4 + 2 * kStages);      // P(j).V(j) done
   const uint32_t b_drain = smem_u32(bars + 5 + 2 * kStages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 6 + 2 * kStages);
+  // O final: committed once, after the last P.V.  (b_o cannot serve: when the
+  // softmax finishes its last tile, the P.V of the tile before it may still be
+  // running, and a parity wait cannot tell three phase counts apart.)
+  const uint32_t b_of = smem_u32(bars + 6 + 2 * kStages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 7 + 2 * kStages);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   if (*reinterpret_cast<volatile int*>(p.status) != 0) return;
@@ -123,6 +127,7 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(b_p, 4);  // one arrival per softmax warp
     mbar_init(b_o, 1);
     mbar_init(b_drain, 1);
+    mbar_init(b_of, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -232,6 +237,7 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         ok = pv(j);
       }
+      if (ok) umma_commit(b_of);  // every P.V done: O is final
       if (!ok) {  // let issued MMAs finish before tensor memory is released
         umma_commit(b_drain);
         mbar_wait_drain(b_drain, 0);
@@ -345,7 +351,10 @@ __global__ void __launch_bounds__(256, 1)
         exact = true;
       }
       if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-        // O holds P.V of tiles 0 .. j-1 once P(j-1).V(j-1) has completed
+        // O holds P.V of tiles 0 .. j-1 once P(j-1).V(j-1) has completed.  S(j)
+        // was committed after P(j-2).V(j-2) was issued and P(j).V(j) waits for
+        // this warpgroup, so b_o has completed j-1 or j phases: a parity wait
+        // on phase j-1 is exact.
         if (!mbar_wait(b_o, (uint32_t)(j - 1) & 1u, ab, 136)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -369,7 +378,7 @@ __global__ void __launch_bounds__(256, 1)
     ok = __all_sync(0xffffffffu, ok);
     if (ok && (n > 0 || (it.flags & kFirstStep))) {
       if (n > 0) {
-        ok = mbar_wait(b_o, (uint32_t)(n - 1) & 1u, ab, 137);  // O final
+        ok = mbar_wait(b_of, 0, ab, 137);  // O final
         tc_fence_after();
       }
       ok = __all_sync(0xffffffffu, ok);
