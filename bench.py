@@ -336,6 +336,8 @@ def main():
     ap.add_argument("--workload", default="long_128k")
     ap.add_argument("--layout", default=None, choices=["zigzag", "contiguous"],
                     help="override the workload's shard layout (same inputs)")
+    ap.add_argument("--tokens", type=int, default=0,
+                    help="a shorter single-document workload of the same shape (profiling small cases)")
     ap.add_argument("--e2e-steps", type=int, default=8)
     # ~12 s of fp64 oracle work per sample on a 16-core host at the 128K shape
     ap.add_argument("--cpu-tokens", type=int, default=40960)
@@ -348,6 +350,10 @@ def main():
     wl = workload(args.workload)
     if args.layout and args.layout != wl.layout:
         wl = dataclasses.replace(wl, layout=args.layout, name="%s_%s" % (wl.name, args.layout))
+    if args.tokens:
+        if wl.num_docs != 1:
+            raise SystemExit("--tokens applies to single-document workloads")
+        wl = dataclasses.replace(wl, T=args.tokens, cu_seqlens=(0, args.tokens), name="%s_T%d" % (wl.name, args.tokens))
     if args.impl == "reference":
         return run_reference(args, wl)
 

@@ -20,7 +20,8 @@
 // from tensor memory).
 //
 // Warp roles (384 threads):
-//   warp 0       producer: K, V once; per pair Q_i with its LSE/Delta slices, dO_i
+//   warp 0       producer: K, V once; per pair Q_i with its LSE/Delta slices and dO_i,
+//                each in two column halves released separately
 //   warp 1       TMEM owner + single-thread UMMA issuer
 //   warps 4-7    compute: P^T (tensor memory), dS^T (shared memory); TMEM lanes = keys;
 //                every kChain pairs, and at the end, they add dK_c, dV_c into the
@@ -89,20 +90,24 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t sK = s0 + kK, sV = s0 + kV, sQ = s0 + kQ, sDO = s0 + kDO, sDS = s0 + kDS, sStg = s0 + kStg;
   float* stat = reinterpret_cast<float*>(smem + kStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kBar);
+  // Q and dO tiles go in two column halves with barriers of their own: the
+  // half a CTA does not use for dV/dK ("other") is free as soon as S (or dP)
+  // has read it, so the next tile's half loads early and S_{i+1} starts on it
+  // while the own half (freed by dK / dV) is still coming.
   const uint32_t b_kv = smem_u32(bars + 0);
-  const uint32_t b_qfull = smem_u32(bars + 1);    // Q_i + LSE/Delta landed
-  const uint32_t b_qempty = smem_u32(bars + 2);   // Q released (after S_i and dK_i)
-  const uint32_t b_dofull = smem_u32(bars + 3);   // dO_i landed
-  const uint32_t b_doempty = smem_u32(bars + 4);  // dO released (after dP_i and dV_i)
-  const uint32_t b_s = smem_u32(bars + 5);        // S^T_i in tensor memory
-  const uint32_t b_dp = smem_u32(bars + 6);       // dP^T_i in tensor memory
-  const uint32_t b_p = smem_u32(bars + 7);        // P^T_i packed in tensor memory
-  const uint32_t b_ds = smem_u32(bars + 8);       // dS^T_i written to shared memory
-  const uint32_t b_dq = smem_u32(bars + 9);       // dQ_i^T in tensor memory
-  const uint32_t b_dqf = smem_u32(bars + 10);     // dQ_i^T read out
-  const uint32_t b_dsf = smem_u32(bars + 11);     // dK_i and dQ_i^T done (dS buffer free)
-  const uint32_t b_drain = smem_u32(bars + 12);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 13);
+  const uint32_t b_qfull = smem_u32(bars + 1);    // [2] Q_i column half landed (own half: + LSE/Delta)
+  const uint32_t b_qempty = smem_u32(bars + 3);   // [2] Q column half released (other: after S_i; own: after dK_i)
+  const uint32_t b_dofull = smem_u32(bars + 5);   // [2] dO_i column half landed
+  const uint32_t b_doempty = smem_u32(bars + 7);  // [2] dO column half released (other: after dP_i; own: after dV_i)
+  const uint32_t b_s = smem_u32(bars + 9);        // S^T_i in tensor memory
+  const uint32_t b_dp = smem_u32(bars + 10);      // dP^T_i in tensor memory
+  const uint32_t b_p = smem_u32(bars + 11);       // P^T_i packed in tensor memory
+  const uint32_t b_ds = smem_u32(bars + 12);      // dS^T_i written to shared memory
+  const uint32_t b_dq = smem_u32(bars + 13);      // dQ_i^T in tensor memory
+  const uint32_t b_dqf = smem_u32(bars + 14);     // dQ_i^T read out
+  const uint32_t b_dsf = smem_u32(bars + 15);     // dK_i and dQ_i^T done (dS buffer free)
+  const uint32_t b_drain = smem_u32(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
   int* abort_flag = reinterpret_cast<int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -119,8 +124,10 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    mbar_init(b_qfull, 1); mbar_init(b_qempty, 1);
-    mbar_init(b_dofull, 1); mbar_init(b_doempty, 1);
+    for (int x = 0; x < 2; ++x) {
+      mbar_init(b_qfull + 8 * x, 1); mbar_init(b_qempty + 8 * x, 1);
+      mbar_init(b_dofull + 8 * x, 1); mbar_init(b_doempty + 8 * x, 1);
+    }
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
     mbar_init(b_p, 4); mbar_init(b_ds, 4);  // one arrival per compute warp
     mbar_init(b_dq, 1); mbar_init(b_dqf, 4);
@@ -150,7 +157,9 @@ __global__ void __launch_bounds__(384, 1)
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------- producer
       bool ok = true;
-      int issued_q = 0, issued_do = 0;
+      int issued = 0;  // pairs whose four loads were all issued
+      int partial = 0;  // loads issued for the pair in progress (0..4)
+      const int own = half, oth = 1 - half;
       tma_prefetch_desc(&tmQ); tma_prefetch_desc(&tmK); tma_prefetch_desc(&tmV); tma_prefetch_desc(&tmDO);
       tma_prefetch_desc(&tmL); tma_prefetch_desc(&tmD);
       mbar_expect_tx(b_kv, 2 * 65536);
@@ -158,18 +167,35 @@ __global__ void __launch_bounds__(384, 1)
         tma_load_3d(sK + b * 16384, &tmK, b_kv, 64 * b, g, it.k0);
         tma_load_3d(sV + b * 16384, &tmV, b_kv, 64 * b, g, it.k0);
       }
-      for (int i = 0; i < npairs; ++i) {
+      // one column half (two 64-column boxes) of a 64-row Q or dO tile
+      auto load_half = [&](uint32_t dst, const CUtensorMap* m, uint32_t bar, int x, int h, int q0) {
+        for (int b = 0; b < 2; ++b) tma_load_3d(dst + (2 * x + b) * 8192, m, bar, 64 * (2 * x + b), h, q0);
+      };
+      for (int i = 0; i < npairs && ok; ++i) {
         const int h = pl.head(i), q0 = pl.start(i);
-        if (!mbar_wait(b_qempty, (i & 1) ^ 1, ab, 241)) { ok = false; break; }
-        mbar_expect_tx(b_qfull, 32768 + 2 * 256);
-        for (int b = 0; b < 4; ++b) tma_load_3d(sQ + b * 8192, &tmQ, b_qfull, 64 * b, h, q0);
-        tma_load_2d(smem_u32(stat), &tmL, b_qfull, q0, h);
-        tma_load_2d(smem_u32(stat + 64), &tmD, b_qfull, q0, h);
-        ++issued_q;
-        if (!mbar_wait(b_doempty, (i & 1) ^ 1, ab, 242)) { ok = false; break; }
-        mbar_expect_tx(b_dofull, 32768);
-        for (int b = 0; b < 4; ++b) tma_load_3d(sDO + b * 8192, &tmDO, b_dofull, 64 * b, h, q0);
-        ++issued_do;
+        const uint32_t ph = (uint32_t)(i & 1) ^ 1u;
+        partial = 0;
+        // in the order the previous pair releases them: Q other (after S),
+        // dO other (after dP), dO own (after dV), Q own with LSE/Delta (after dK)
+        if (!mbar_wait(b_qempty + 8 * oth, ph, ab, 241)) { ok = false; break; }
+        mbar_expect_tx(b_qfull + 8 * oth, 16384);
+        load_half(sQ, &tmQ, b_qfull + 8 * oth, oth, h, q0);
+        ++partial;
+        if (!mbar_wait(b_doempty + 8 * oth, ph, ab, 242)) { ok = false; break; }
+        mbar_expect_tx(b_dofull + 8 * oth, 16384);
+        load_half(sDO, &tmDO, b_dofull + 8 * oth, oth, h, q0);
+        ++partial;
+        if (!mbar_wait(b_doempty + 8 * own, ph, ab, 242)) { ok = false; break; }
+        mbar_expect_tx(b_dofull + 8 * own, 16384);
+        load_half(sDO, &tmDO, b_dofull + 8 * own, own, h, q0);
+        ++partial;
+        if (!mbar_wait(b_qempty + 8 * own, ph, ab, 241)) { ok = false; break; }
+        mbar_expect_tx(b_qfull + 8 * own, 16384 + 2 * 256);
+        load_half(sQ, &tmQ, b_qfull + 8 * own, own, h, q0);
+        tma_load_2d(smem_u32(stat), &tmL, b_qfull + 8 * own, q0, h);
+        tma_load_2d(smem_u32(stat + 64), &tmD, b_qfull + 8 * own, q0, h);
+        partial = 0;
+        ++issued;
       }
       {
         // the CTA that takes this SM next: its K/V tile into L2 now
@@ -185,8 +211,12 @@ __global__ void __launch_bounds__(384, 1)
       }
       if (!ok) {  // drain this CTA's copies still in flight
         mbar_wait_drain(b_kv, 0);
-        if (issued_q > 0) mbar_wait_drain(b_qfull, (issued_q - 1) & 1);
-        if (issued_do > 0) mbar_wait_drain(b_dofull, (issued_do - 1) & 1);
+        const uint32_t bars4[4] = {b_qfull + 8 * (uint32_t)oth, b_dofull + 8 * (uint32_t)oth,
+                                   b_dofull + 8 * (uint32_t)own, b_qfull + 8 * (uint32_t)own};
+        for (int x = 0; x < 4; ++x) {
+          const int n = issued + (x < partial ? 1 : 0);  // loads issued on this barrier
+          if (n > 0) mbar_wait_drain(bars4[x], (uint32_t)(n - 1) & 1u);
+        }
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -196,20 +226,33 @@ __global__ void __launch_bounds__(384, 1)
       for (int i = 0; i < npairs && ok; ++i) {
         const uint32_t pi = (uint32_t)i & 1u;
         const bool chain_start = (i % kChain) == 0;
-        if (!mbar_wait(b_qfull, pi, ab, 244) || !mbar_wait(b_dofull, pi, ab, 245)) { ok = false; break; }
+        // S^T = K Q^T and dP^T = V dO^T over the 256 columns, the other
+        // column half first (it lands first), releasing it right away
+        const int oth = 1 - half;
+        auto s_half = [&](uint32_t d, uint32_t a, uint32_t bq, int x, bool first) {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const int gk = 8 * x + k;
+            const uint32_t ko = (gk >> 2) * 16384 + (gk & 3) * 32, qo = (gk >> 2) * 8192 + (gk & 3) * 32;
+            umma_ss(d, sdesc_sw128(a + ko, 16, 1024), sdesc_sw128(bq + qo, 16, 1024), kIdescS,
+                    (first && k == 0) ? 0u : 1u);
+          }
+        };
+        if (!mbar_wait(b_qfull + 8 * oth, pi, ab, 244)) { ok = false; break; }
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T over the 256 columns
-#pragma unroll
-        for (int gk = 0; gk < 16; ++gk) {
-          const uint32_t ko = (gk >> 2) * 16384 + (gk & 3) * 32, qo = (gk >> 2) * 8192 + (gk & 3) * 32;
-          umma_ss(tmem + tS, sdesc_sw128(sK + ko, 16, 1024), sdesc_sw128(sQ + qo, 16, 1024), kIdescS, gk > 0);
-        }
+        s_half(tmem + tS, sK, sQ, oth, true);
+        umma_commit(b_qempty + 8 * oth);
+        if (!mbar_wait(b_qfull + 8 * half, pi, ab, 244)) { ok = false; break; }
+        tc_fence_after();
+        s_half(tmem + tS, sK, sQ, half, false);
         umma_commit(b_s);
-#pragma unroll
-        for (int gk = 0; gk < 16; ++gk) {
-          const uint32_t ko = (gk >> 2) * 16384 + (gk & 3) * 32, qo = (gk >> 2) * 8192 + (gk & 3) * 32;
-          umma_ss(tmem + tP, sdesc_sw128(sV + ko, 16, 1024), sdesc_sw128(sDO + qo, 16, 1024), kIdescS, gk > 0);
-        }
+        if (!mbar_wait(b_dofull + 8 * oth, pi, ab, 245)) { ok = false; break; }
+        tc_fence_after();
+        s_half(tmem + tP, sV, sDO, oth, true);
+        umma_commit(b_doempty + 8 * oth);
+        if (!mbar_wait(b_dofull + 8 * half, pi, ab, 245)) { ok = false; break; }
+        tc_fence_after();
+        s_half(tmem + tP, sV, sDO, half, false);
         umma_commit(b_dp);
         // dV_c += P^T dO_c once P^T is packed (A from tensor memory; B MN-major,
         // the half's two 64-column boxes 8 KB apart)
@@ -219,7 +262,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < 4; ++kk)
           umma_ts(tmem + tdV, tmem + tS + kk * 8, sdesc_sw128(dO_c + kk * 2048, 8192, 1024), kIdescG,
                   (!chain_start || kk > 0) ? 1u : 0u);
-        umma_commit(b_doempty);
+        umma_commit(b_doempty + 8 * half);
         // dK_c += dS^T Q_c once dS^T is in shared memory
         if (!mbar_wait(b_ds, pi, ab, 247)) { ok = false; break; }
         tc_fence_after();
@@ -227,7 +270,7 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < 4; ++kk)
           umma_ss(tmem + tdK, sdesc_sw128(sDS + kk * 32, 16, 1024), sdesc_sw128(Q_c + kk * 2048, 8192, 1024),
                   kIdescG, (!chain_start || kk > 0) ? 1u : 0u);
-        umma_commit(b_qempty);
+        umma_commit(b_qempty + 8 * half);
         // dQ_c^T = K_c^T dS^T once the previous one has left tensor memory
         if (i > 0 && !mbar_wait(b_dqf, pi ^ 1u, ab, 248)) { ok = false; break; }
         tc_fence_after();
