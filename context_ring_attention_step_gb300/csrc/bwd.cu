@@ -215,22 +215,27 @@ __global__ void __launch_bounds__(512, 1)
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
+      // Every operand descriptor is the shared-memory base's plus constants
+      // (sdesc_at): each MMA costs two adds to issue, so the single issuing
+      // thread keeps up with the tensor pipe.  K-major operands: lbo 16;
+      // MN-major: lbo = the 64-column block stride.
+      const uint64_t d0 = sdesc_sw128(s0, 0, 1024);
       auto issue_s = [&](int i) {  // S^T_i = K Q_i^T
-        const uint32_t sq = sQ + (i & 1) * C::kTile;
+        const uint64_t dk = opaque(d0);
+        const uint64_t dq = sdesc_at(dk, (uint32_t)(i & 1) * C::kTile, 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::tS, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(sq + off, 16, 1024), C::kIdescS,
-                  kk > 0);
+          umma_ss(tmem + C::tS, sdesc_at(dk, C::kK + off, 16), sdesc_at(dq, C::kQ0 + off, 16), C::kIdescS, kk > 0);
         }
         umma_commit(b_s);
       };
       auto issue_dp = [&]() {  // dP^T = V dO^T
+        const uint64_t dv = opaque(d0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::tP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(sDO + off, 16, 1024), C::kIdescS,
-                  kk > 0);
+          umma_ss(tmem + C::tP, sdesc_at(dv, C::kV + off, 16), sdesc_at(dv, C::kDO + off, 16), C::kIdescS, kk > 0);
         }
         umma_commit(b_dp);
       };
@@ -246,7 +251,8 @@ __global__ void __launch_bounds__(512, 1)
       for (int i = 0; i < npairs && ok; ++i) {
         const int st = i & 1;
         const uint32_t pi = i & 1;
-        const uint32_t sq = sQ + st * C::kTile;
+        const uint64_t db = opaque(d0);
+        const uint64_t dq = sdesc_at(db, (uint32_t)st * C::kTile, 0);  // this pair's Q stage
         // dV += P^T dO once P_i is packed (A from tensor memory: query columns
         // 0-63 in columns [0,32) of the S region, 64-127 in [64,96); B MN-major)
         if (!mbar_wait(b_p, pi, ab, 205)) { ok = false; break; }
@@ -256,8 +262,8 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8,
-                  sdesc_sw128(sDO + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(db, C::kDO + kk * 2048, 16384),
+                  C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_doempty);
         // S_{i+1} right behind dV_i, the last reader of P_i in the S region
         if (i + 1 < npairs) {
@@ -271,13 +277,13 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::tP, sdesc_sw128(sDS + kk * 2048, 16384, 1024), sdesc_sw128(sK + kk * 2048, 16384, 1024),
+          umma_ss(tmem + C::tP, sdesc_at(db, C::kDS + kk * 2048, 16384), sdesc_at(db, C::kK + kk * 2048, 16384),
                   C::kIdescQ, kk > 0);
         umma_commit(b_dq);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ss(tmem + C::tdK, sdesc_sw128(sDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                  sdesc_sw128(sq + kk * 2048, 16384, 1024), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
+          umma_ss(tmem + C::tdK, sdesc_at(db, C::kDS + (kk >> 2) * 16384 + (kk & 3) * 32, 16),
+                  sdesc_at(dq, C::kQ0 + kk * 2048, 16384), C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
         umma_commit(b_qempty + 8 * st);
         umma_commit(b_dsf);
         // dP_{i+1} once dQ_i has left the region and dO_{i+1} has landed

@@ -236,18 +236,23 @@ __global__ void __launch_bounds__(384, 1)
       const bool my_qa = qt == 0 ? q_act[0] : q_act[1];
       const int my_last = qt == 0 ? last_row[0] : last_row[1];
       auto act = [&](int j) { return active(j, my_qa, my_last, na); };
-      const uint32_t tS = tmem + qt * 128, tO = tmem + 256 + qt * D, qa = sQ + qt * C::kTile;
+      const uint32_t tS = tmem + qt * 128, tO = tmem + 256 + qt * D;
       bool ok = mbar_wait(b_q, 0, ab, 102);
       tc_fence_after();
       int stage = 0;
       uint32_t kph = 0;
       auto advance = [&]() { if (++stage == C::kStages) { stage = 0; kph ^= 1; } };
+      // Every operand descriptor is the shared-memory base's plus constants
+      // (sdesc_at), so each MMA costs an add or two to issue.
+      const uint64_t d0 = sdesc_sw128(sQ, 0, 1024);
       auto qk = [&](int kst) {
-        const uint32_t ka = sKV + kst * C::kTile;
+        const uint64_t b = opaque(d0);
+        const uint64_t dq = sdesc_at(b, (uint32_t)qt * C::kTile, 0);
+        const uint64_t dk = sdesc_at(b, (uint32_t)(C::kQBytes + kst * C::kTile), 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tS, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(ka + off, 16, 1024), C::kIdescQK, kk > 0);
+          umma_ss(tS, sdesc_at(dq, off, 16), sdesc_at(dk, off, 16), C::kIdescQK, kk > 0);
         }
       };
       // b_s is committed right after each QK of a tile this Q tile sees (S
@@ -271,11 +276,10 @@ __global__ void __launch_bounds__(384, 1)
           if (!mbar_wait(b_p + 8 * qt, pph, ab, 105)) { ok = false; break; }
           pph ^= 1;
           tc_fence_after();
-          const uint32_t va = sKV + vst * C::kTile;
+          const uint64_t dv = sdesc_at(opaque(d0), (uint32_t)(C::kQBytes + vst * C::kTile), 0);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tO, tS + kk * 8, sdesc_sw128(va + kk * 2048, 16384, 1024), C::kIdescPV,
-                    (u > 0 || kk > 0) ? 1u : 0u);
+            umma_ts(tO, tS + kk * 8, sdesc_at(dv, kk * 2048, 16384), C::kIdescPV, (u > 0 || kk > 0) ? 1u : 0u);
           if (++u == na) umma_commit(b_s + 8 * qt);  // O final
         }
         umma_commit(b_empty + 8 * vst);  // V_j: free once this tile's P.V has run

@@ -192,19 +192,22 @@ __global__ void __launch_bounds__(256, 1)
         return mbar_wait(b_full + 8 * (idx % kStages), (idx / kStages) & 1, ab, 133);
       };
       // S(j) = Q K(j)^T into buffer j & 1
+      // Every operand descriptor is the shared-memory base's plus constants
+      // (sdesc_at), so each MMA costs an add or two to issue.
+      const uint64_t d0 = sdesc_sw128(sQ, 0, 1024);
       auto qk = [&](int j) -> bool {
         const uint32_t tS = tmem + (uint32_t)(j & 1) * 128;
         for (int half = 0; half < 2; ++half) {
           if (!wait_full(c)) return false;
           tc_fence_after();
-          const uint32_t kb = sKV + (c % kStages) * kHalfTile;
+          const uint64_t b = opaque(d0);
+          const uint64_t dk = sdesc_at(b, (uint32_t)(kQBytes + (c % kStages) * kHalfTile), 0);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk) {
             const int gk = 8 * half + kk;  // K step over the 256 columns of Q
             const uint32_t qoff = (gk >> 2) * 16384 + (gk & 3) * 32;
             const uint32_t koff = (kk >> 2) * 16384 + (kk & 3) * 32;
-            umma_ss(tS, sdesc_sw128(sQ + qoff, 16, 1024), sdesc_sw128(kb + koff, 16, 1024), kIdescQK,
-                    (half | kk) ? 1u : 0u);
+            umma_ss(tS, sdesc_at(b, qoff, 16), sdesc_at(dk, koff, 16), kIdescQK, (half | kk) ? 1u : 0u);
           }
           umma_commit(b_empty + 8 * (c % kStages));  // the half tile is free once these MMAs ran
           ++c;
@@ -219,10 +222,10 @@ __global__ void __launch_bounds__(256, 1)
         for (int half = 0; half < 2; ++half) {
           if (!wait_full(c)) return false;
           tc_fence_after();
-          const uint32_t vb = sKV + (c % kStages) * kHalfTile;
+          const uint64_t dv = sdesc_at(opaque(d0), (uint32_t)(kQBytes + (c % kStages) * kHalfTile), 0);
 #pragma unroll
           for (int kk = 0; kk < 8; ++kk)
-            umma_ts(tmem + 256 + 128 * half, tS + kk * 8, sdesc_sw128(vb + kk * 2048, 16384, 1024), kIdescPV,
+            umma_ts(tmem + 256 + 128 * half, tS + kk * 8, sdesc_at(dv, kk * 2048, 16384), kIdescPV,
                     (j > 0 || kk > 0) ? 1u : 0u);
           umma_commit(b_empty + 8 * (c % kStages));
           ++c;

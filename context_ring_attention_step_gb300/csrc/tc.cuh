@@ -277,6 +277,23 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
 
+// Descriptor of the operand `off` bytes past `base` with leading byte offset
+// `lbo`, from the descriptor of `base` built with lbo = 0 (same swizzle and
+// stride).  Only the start and leading-offset fields change: shared-memory
+// addresses stay below 256 KB and offsets below 256 KB, so neither 14-bit
+// field carries into the next one and a plain add is exact.  With `off` and
+// `lbo` known at compile time, an operand costs one add to issue.
+__device__ __forceinline__ uint64_t sdesc_at(uint64_t base_desc, uint32_t off, uint32_t lbo) {
+  return base_desc + (uint64_t)(off >> 4) + ((uint64_t)(lbo >> 4) << 16);
+}
+// An opaque copy: descriptors derived from it are computed where they are
+// used (one add each) instead of being hoisted out of a loop and held in
+// registers.
+__device__ __forceinline__ uint64_t opaque(uint64_t x) {
+  asm volatile("" : "+l"(x));
+  return x;
+}
+
 // TMEM address: lane in [31:16], column in [15:0].
 __device__ __forceinline__ uint32_t tmem_addr(uint32_t base, uint32_t lane, uint32_t col) {
   return base + (lane << 16) + col;
