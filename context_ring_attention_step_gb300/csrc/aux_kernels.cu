@@ -1,7 +1,9 @@
 // aux_kernels.cu -- the HBM-bound passes around the ring steps:
 //   * cast of the fp32 running output to the bf16 result (forward finalise);
 //   * backward preprocess: Delta = rowsum(dO * O) with 8-lane shuffle
-//     reductions, and LSE rescaled to log2 units for the exp2-based recompute.
+//     reductions, and LSE rescaled to log2 units for the exp2-based recompute;
+//     both stored negated (-Delta, -LSE log2e), the form the backward kernels
+//     add with packed fp32 arithmetic.
 #include <cuda_bf16.h>
 
 #include <algorithm>
@@ -107,8 +109,8 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ o, int o_fp32, co
   if (row < rows && sub == 0) {
     const int t = (int)(row / Hq), h = (int)(row % Hq);
     const size_t idx = (size_t)h * pitch + t;
-    delta[idx] = acc;
-    lse2[idx] = lse[(size_t)h * T + t] * kLog2e;
+    delta[idx] = -acc;
+    lse2[idx] = -lse[(size_t)h * T + t] * kLog2e;
   }
 }
 

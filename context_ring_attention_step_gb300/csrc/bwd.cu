@@ -311,7 +311,7 @@ __global__ void __launch_bounds__(512, 1)
     const uint32_t tS = tmem_addr(tmem, lane_base, C::tS);
     const uint32_t tP = tmem_addr(tmem, lane_base, C::tP);
     const int krow = it.k0 + tid;
-    const float sl2 = p.scale_log2, scale = p.scale;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2), scale2 = f2_pack(p.scale, p.scale);
     constexpr int DH = D / 2;  // head-dim columns per warpgroup
     const uint32_t row_addr = sDS + wg * 16384 + tid * 128;
     // add this warpgroup's half of dV and dK (tensor memory, lanes = key rows)
@@ -347,11 +347,11 @@ __global__ void __launch_bounds__(512, 1)
       cmin = (krow >= it.k1) ? 128 : max(qlo - q0, p.causal ? krow - q0 : 0);
       cmax = qe - q0;  // exclusive
     };
-    // P^T of the current pair in fp32 (masked), kept for its dS phase: dS is
-    // formed from the unrounded P, so it carries one bf16 rounding (its own,
-    // for the dK/dQ MMAs) instead of two; only the dV MMA consumes the
-    // bf16-rounded P.
-    float pf[64];
+    // P^T of the current pair times the softmax scale, as packed fp32 pairs
+    // (masked), kept for its dS phase: dS is formed from the unrounded P, so
+    // it carries one bf16 rounding (its own, for the dK/dQ MMAs) instead of
+    // two; only the dV MMA consumes the bf16-rounded P.
+    uint64_t pf[32];
     // ---- P^T = exp2(S^T scale log2e - LSE log2e) on columns [64 wg, 64 wg + 64),
     // packed into this warpgroup's own columns of the S region (never into the
     // other warpgroup's columns, which it may not have read yet)
@@ -368,28 +368,25 @@ __global__ void __launch_bounds__(512, 1)
       tmem_ld_wait();
       reg_fence32(r[0]);
       reg_fence32(r[1]);
+      uint32_t w0[16], w1[16];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 64 * wg + 32 * c + 2 * x;
-          const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' LSE
-          const float la = (x & 1) ? l4.z : l4.x, lb = (x & 1) ? l4.w : l4.y;
-          float p0 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x]), sl2, -la));
-          float p1 = ex2_approx(fmaf(__uint_as_float(r[c][2 * x + 1]), sl2, -lb));
+          const float4 l4 = sl4[c0 >> 2];  // broadcast read of 4 columns' -LSE log2e
+          const uint64_t nl = (x & 1) ? f2_pack(l4.z, l4.w) : f2_pack(l4.x, l4.y);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[c][2 * x]), __uint_as_float(r[c][2 * x + 1])), sl2x2, nl), x0,
+                    x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (need_mask) {
             if (c0 < cmin || c0 >= cmax) p0 = 0.f;
             if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
           }
-          pf[32 * c + 2 * x] = p0;
-          pf[32 * c + 2 * x + 1] = p1;
+          pf[16 * c + x] = f2_mul(f2_pack(p0, p1), scale2);
+          (c == 0 ? w0 : w1)[x] = pack_bf16x2(p0, p1);
         }
-      }
-      uint32_t w0[16], w1[16];
-#pragma unroll
-      for (int x = 0; x < 16; ++x) {
-        w0[x] = pack_bf16x2(pf[2 * x], pf[2 * x + 1]);
-        w1[x] = pack_bf16x2(pf[32 + 2 * x], pf[32 + 2 * x + 1]);
       }
       tmem_st16(tS + 64 * wg, w0);
       tmem_st16(tS + 64 * wg + 16, w1);
@@ -418,10 +415,12 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 64 * wg + 32 * c + 2 * x;
-          const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' Delta
-          const float da = (x & 1) ? d4.z : d4.x, db = (x & 1) ? d4.w : d4.y;
-          const float d0 = pf[32 * c + 2 * x] * (__uint_as_float(r[c][2 * x]) - da) * scale;
-          const float d1 = pf[32 * c + 2 * x + 1] * (__uint_as_float(r[c][2 * x + 1]) - db) * scale;
+          const float4 d4 = sl4[32 + (c0 >> 2)];  // broadcast read of 4 columns' -Delta
+          const uint64_t nd = (x & 1) ? f2_pack(d4.z, d4.w) : f2_pack(d4.x, d4.y);
+          float d0, d1;  // scale P (dP - Delta)
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(r[c][2 * x]), __uint_as_float(r[c][2 * x + 1])), nd),
+                           pf[16 * c + x]),
+                    d0, d1);
           w[c][x] = pack_bf16x2(d0, d1);
         }
       }

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(384, 1)
             const float la[4] = {l.x, l.y, l.z, l.w};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-              const float pv = ex2_approx(fmaf(__uint_as_float(r[c][x + e]), sl2, -la[e]));
+              const float pv = ex2_approx(fmaf(__uint_as_float(r[c][x + e]), sl2, la[e]));  // la = -LSE log2e
               pf[c0 + e] = (c0 + e < cmin || c0 + e >= cmax) ? 0.f : pv;
             }
           }
@@ -379,10 +379,11 @@ __global__ void __launch_bounds__(384, 1)
           for (int x = 0; x < 32; x += 4) {
             const int c0 = 32 * c + x;
             const float4 d = d4[c0 >> 2];
-            const float v0 = pf[c0] * (__uint_as_float(r[c][x]) - d.x) * scale;
-            const float v1 = pf[c0 + 1] * (__uint_as_float(r[c][x + 1]) - d.y) * scale;
-            const float v2 = pf[c0 + 2] * (__uint_as_float(r[c][x + 2]) - d.z) * scale;
-            const float v3 = pf[c0 + 3] * (__uint_as_float(r[c][x + 3]) - d.w) * scale;
+            // d = -Delta
+            const float v0 = pf[c0] * (__uint_as_float(r[c][x]) + d.x) * scale;
+            const float v1 = pf[c0 + 1] * (__uint_as_float(r[c][x + 1]) + d.y) * scale;
+            const float v2 = pf[c0 + 2] * (__uint_as_float(r[c][x + 2]) + d.z) * scale;
+            const float v3 = pf[c0 + 3] * (__uint_as_float(r[c][x + 3]) + d.w) * scale;
             w[c0 / 2] = pack_bf16x2(v0, v1);
             w[c0 / 2 + 1] = pack_bf16x2(v2, v3);
           }
