@@ -19,18 +19,20 @@
 // (P^T from the unrounded fp32 P for dS; the bf16-rounded P feeds the dV MMA
 // from tensor memory).
 //
-// Warp roles (384 threads):
+// Warp roles (512 threads):
 //   warp 0       producer: K, V once; per pair Q_i with its LSE/Delta slices and dO_i,
 //                each in two column halves released separately
 //   warp 1       TMEM owner + single-thread UMMA issuer
-//   warps 4-7    compute: P^T (tensor memory), dS^T (shared memory); TMEM lanes = keys;
+//   warps 4-11   two compute warpgroups, each on half of the 64 query columns:
+//                P^T (tensor memory), dS^T (shared memory); TMEM lanes = keys;
 //                every kChain pairs, and at the end, they add dK_c, dV_c into the
-//                fp32 accumulators
-//   warps 8-11   dQ: read dQ_c^T out of tensor memory (lanes = columns), stage it
+//                fp32 accumulators (each warpgroup half of the columns)
+//   warps 12-15  dQ: read dQ_c^T out of tensor memory (lanes = columns), stage it
 //                per warp as 32 query rows x 32 columns and add it into the fp32
 //                accumulator with bulk tensor reductions
 // Tensor memory: dV_c [0,128), dK_c [128,256), S^T/P^T [256,320), dP^T [320,384),
-// dQ_c^T [384,448).
+// dQ_c^T [384,448).  P^T (bf16, two per column) overwrites columns [0,16) and
+// [32,48) of S^T, each warpgroup in its own columns.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
 
@@ -74,7 +76,7 @@ __device__ __forceinline__ void red_add4(float* addr, float a, float b, float c,
                : "memory");
 }
 
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     ring_bwd_d256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                          const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                          const __grid_constant__ CUtensorMap tmL, const __grid_constant__ CUtensorMap tmD,
@@ -129,7 +131,7 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(b_dofull + 8 * x, 1); mbar_init(b_doempty + 8 * x, 1);
     }
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
-    mbar_init(b_p, 4); mbar_init(b_ds, 4);  // one arrival per compute warp
+    mbar_init(b_p, 8); mbar_init(b_ds, 8);  // one arrival per compute warp (two warpgroups)
     mbar_init(b_dq, 1); mbar_init(b_dqf, 4);
     mbar_init(b_dsf, 1);
     mbar_init(b_drain, 1);
@@ -149,9 +151,9 @@ __global__ void __launch_bounds__(384, 1)
     return __all_sync(0xffffffffu, mbar_wait(bar, parity, ab, site)) != 0;
   };
 
-  // Register split: 384 threads x 168 at launch.  Producer/MMA warpgroup 88
-  // (its unrolled MMA loop spills below that), compute warpgroup 216, dQ
-  // warpgroup 104: 128 x (88 + 216 + 104) = 52224 <= 64512.
+  // Register split: 512 threads x 128 at launch.  Producer/MMA warpgroup 88
+  // (its unrolled MMA loop spills below that), compute warpgroups 152, dQ
+  // warpgroup 104: 128 x (88 + 2 x 152 + 104) = 63488 <= 65536.
   if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;");
     if (warp == 0 && lane == 0) {
@@ -254,14 +256,15 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         s_half(tmem + tP, sV, sDO, half, false);
         umma_commit(b_dp);
-        // dV_c += P^T dO_c once P^T is packed (A from tensor memory; B MN-major,
-        // the half's two 64-column boxes 8 KB apart)
+        // dV_c += P^T dO_c once P^T is packed (A from tensor memory: query
+        // columns 0-31 in columns [0,16) of the S region, 32-63 in [32,48);
+        // B MN-major, the half's two 64-column boxes 8 KB apart)
         if (!mbar_wait(b_p, pi, ab, 246)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          umma_ts(tmem + tdV, tmem + tS + kk * 8, sdesc_sw128(dO_c + kk * 2048, 8192, 1024), kIdescG,
-                  (!chain_start || kk > 0) ? 1u : 0u);
+          umma_ts(tmem + tdV, tmem + tS + (kk >> 1) * 32 + (kk & 1) * 8, sdesc_sw128(dO_c + kk * 2048, 8192, 1024),
+                  kIdescG, (!chain_start || kk > 0) ? 1u : 0u);
         umma_commit(b_doempty + 8 * half);
         // dK_c += dS^T Q_c once dS^T is in shared memory
         if (!mbar_wait(b_ds, pi, ab, 247)) { ok = false; break; }
@@ -286,23 +289,32 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait_drain(b_drain, 0);
       }
     }
-  } else if (warp < 8) {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 216;");
-    // ------------------------------------------------------------ compute warpgroup
-    const int tid = threadIdx.x - 128;
+  } else if (warp < 12) {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 152;");
+    // ------------------------------------------------------------ compute warpgroups
+    // Two warpgroups split each tile's 64 query columns: warpgroup w takes
+    // columns [32w, 32w + 32) of S^T/dP^T (TMEM lanes = key rows), packs P^T
+    // into tensor-memory columns [32w, 32w + 16) of the S region and writes
+    // 16-byte chunks [4w, 4w + 4) of each dS^T row; at the end each flushes
+    // half of the 128 dK/dV columns.
+    const int wg = (warp - 4) >> 2;
+    const int tid = threadIdx.x - 128 * (1 + wg);
     const uint32_t lane_base = (uint32_t)(warp & 3) * 32;
-    const uint32_t aS = tmem_addr(tmem, lane_base, tS), aP = tmem_addr(tmem, lane_base, tP);
+    const uint32_t aS = tmem_addr(tmem, lane_base, tS + 32 * wg), aP = tmem_addr(tmem, lane_base, tP + 32 * wg);
+    // packed P^T goes into this warpgroup's own S columns (never into the
+    // other warpgroup's, which it may not have read yet)
+    const uint32_t aPk = aS;
     const int krow = it.k0 + tid;
     const bool valid = krow < it.k1;
-    const float sl2 = p.scale_log2, scale = p.scale;
+    const uint64_t sl2x2 = f2_pack(p.scale_log2, p.scale_log2), scale2 = f2_pack(p.scale, p.scale);
     const uint32_t row_addr = sDS + (uint32_t)tid * 128;
     auto flush_dkdv = [&]() {
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
-        const uint32_t t = tmem_addr(tmem, lane_base, which == 0 ? tdV : tdK);
-        float* dst = (which == 0 ? p.dv_acc : p.dk_acc) + ((size_t)krow * p.Hkv + g) * kD + 128 * half;
+        const uint32_t t = tmem_addr(tmem, lane_base, (which == 0 ? tdV : tdK) + 64 * wg);
+        float* dst = (which == 0 ? p.dv_acc : p.dk_acc) + ((size_t)krow * p.Hkv + g) * kD + 128 * half + 64 * wg;
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < 2; ++c) {
           uint32_t r[32];
           tmem_ld32(t + 32 * c, r);
           tmem_ld_wait();
@@ -316,45 +328,37 @@ __global__ void __launch_bounds__(384, 1)
         }
       }
     };
-    float pf[64];  // P^T of the current pair (fp32, masked), for its dS phase
+    uint64_t pf[16];  // scale P^T of this warpgroup's columns (packed fp32 pairs, masked), for its dS phase
     bool ok = true;
     for (int i = 0; i < npairs && ok; ++i) {
       const uint32_t pi = (uint32_t)i & 1u;
-      // ---- P^T = exp2(S^T scale log2e - LSE log2e) on the tile's 64 query columns
+      // ---- P^T = exp2(S^T scale log2e - LSE log2e) on this warpgroup's 32 columns
       if (!wait_warp(b_s, pi, 250)) { ok = false; break; }
       tc_fence_after();
       const int q0 = pl.start(i), qlo = pl.lo(i), qe = pl.end(i);
       const int cmin = valid ? max(qlo - q0, p.causal ? krow - q0 : 0) : 64;
       const int cmax = qe - q0;  // exclusive
       {
-        uint32_t r[2][32];
-        tmem_ld32(aS, r[0]);
-        tmem_ld32(aS + 32, r[1]);
+        uint32_t r[32];
+        tmem_ld32(aS, r);
         tmem_ld_wait();
-        reg_fence32(r[0]);
-        reg_fence32(r[1]);
-        const float4* l4 = reinterpret_cast<const float4*>(stat);
-#pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            const int c0 = 32 * c + x;
-            const float4 l = l4[c0 >> 2];
-            const float la[4] = {l.x, l.y, l.z, l.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float pv = ex2_approx(fmaf(__uint_as_float(r[c][x + e]), sl2, la[e]));  // la = -LSE log2e
-              pf[c0 + e] = (c0 + e < cmin || c0 + e >= cmax) ? 0.f : pv;
-            }
-          }
-        uint32_t w0[16], w1[16];
+        reg_fence32(r);
+        const float4* l4 = reinterpret_cast<const float4*>(stat);  // -LSE log2e
+        uint32_t w[16];
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
-          w0[x] = pack_bf16x2(pf[2 * x], pf[2 * x + 1]);
-          w1[x] = pack_bf16x2(pf[32 + 2 * x], pf[32 + 2 * x + 1]);
+          const int c0 = 32 * wg + 2 * x;
+          const float4 l = l4[c0 >> 2];
+          const uint64_t nl = (x & 1) ? f2_pack(l.z, l.w) : f2_pack(l.x, l.y);
+          float x0, x1;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), sl2x2, nl), x0, x1);
+          float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
+          if (c0 < cmin || c0 >= cmax) p0 = 0.f;
+          if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
+          pf[x] = f2_mul(f2_pack(p0, p1), scale2);
+          w[x] = pack_bf16x2(p0, p1);
         }
-        tmem_st16(aS, w0);
-        tmem_st16(aS + 16, w1);
+        tmem_st16(aPk, w);
         tmem_st_wait();
       }
       tc_fence_before();
@@ -364,42 +368,38 @@ __global__ void __launch_bounds__(384, 1)
       // the previous pair have read the buffer
       if (!wait_warp(b_dp, pi, 251)) { ok = false; break; }
       tc_fence_after();
-      uint32_t w[32];
+      uint32_t w[16];
       {
-        uint32_t r[2][32];
-        tmem_ld32(aP, r[0]);
-        tmem_ld32(aP + 32, r[1]);
+        uint32_t r[32];
+        tmem_ld32(aP, r);
         tmem_ld_wait();
-        reg_fence32(r[0]);
-        reg_fence32(r[1]);
-        const float4* d4 = reinterpret_cast<const float4*>(stat + 64);
+        reg_fence32(r);
+        const float4* d4 = reinterpret_cast<const float4*>(stat + 64);  // -Delta
 #pragma unroll
-        for (int c = 0; c < 2; ++c)
-#pragma unroll
-          for (int x = 0; x < 32; x += 4) {
-            const int c0 = 32 * c + x;
-            const float4 d = d4[c0 >> 2];
-            // d = -Delta
-            const float v0 = pf[c0] * (__uint_as_float(r[c][x]) + d.x) * scale;
-            const float v1 = pf[c0 + 1] * (__uint_as_float(r[c][x + 1]) + d.y) * scale;
-            const float v2 = pf[c0 + 2] * (__uint_as_float(r[c][x + 2]) + d.z) * scale;
-            const float v3 = pf[c0 + 3] * (__uint_as_float(r[c][x + 3]) + d.w) * scale;
-            w[c0 / 2] = pack_bf16x2(v0, v1);
-            w[c0 / 2 + 1] = pack_bf16x2(v2, v3);
-          }
+        for (int x = 0; x < 16; ++x) {
+          const int c0 = 32 * wg + 2 * x;
+          const float4 d = d4[c0 >> 2];
+          const uint64_t nd = (x & 1) ? f2_pack(d.z, d.w) : f2_pack(d.x, d.y);
+          float v0, v1;
+          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), nd), pf[x]), v0,
+                    v1);
+          w[x] = pack_bf16x2(v0, v1);
+        }
       }
       tc_fence_before();  // dP^T is in registers
       if (i > 0 && !wait_warp(b_dsf, pi ^ 1u, 252)) { ok = false; break; }
 #pragma unroll
-      for (int pc = 0; pc < 8; ++pc)
-        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((pc ^ (tid & 7)) << 4)),
+      for (int pc = 0; pc < 4; ++pc) {
+        const int chunk = 4 * wg + pc;
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(row_addr + ((chunk ^ (tid & 7)) << 4)),
                      "r"(w[4 * pc]), "r"(w[4 * pc + 1]), "r"(w[4 * pc + 2]), "r"(w[4 * pc + 3])
                      : "memory");
+      }
       fence_proxy_async_smem();
       __syncwarp();
       if (lane == 0) mbar_arrive(b_ds);
       // a finished dV/dK chain (more pairs follow): into the accumulators before
-      // this warpgroup hands over the next P^T, whose dV starts a new chain
+      // these warpgroups hand over the next P^T, whose dV starts a new chain
       if ((i + 1) % kChain == 0 && i + 1 < npairs) {
         if (!wait_warp(b_dsf, pi, 253)) { ok = false; break; }
         tc_fence_after();
@@ -484,7 +484,7 @@ cudaError_t launch_bwd_step_d256(const CUtensorMap& tq, const CUtensorMap& tk, c
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
   q.next_cta = sms;
-  kern<<<(unsigned)grid, 384, b256::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, q);
+  kern<<<(unsigned)grid, 512, b256::kSmem, stream>>>(tq, tk, tv, tdo, tl, td, tdq, q);
   return cudaGetLastError();
 }
 
