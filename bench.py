@@ -58,7 +58,7 @@ def peaks():
 
 KERNEL_SOURCES = {
     "ring_fwd_step_kernel": ("fwd.cu", "tc.cuh", "ring_attn_internal.h"),
-    "ring_bwd_step_kernel": ("bwd.cu", "tc.cuh", "ring_attn_internal.h"),
+    "ring_bwd_step_kernel": ("bwd.cu", "bwd_tiles.cuh", "tc.cuh", "ring_attn_internal.h"),
 }
 
 
@@ -485,12 +485,49 @@ def main():
     chk(lib.ra_workspace_status(P_(ws_r), sp))
     rs_kernel_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in rev), dist, dev) / args.steps
 
+    # ---------------------------------------------------------------- CTA-pair backward
+    # head_dim 128: the same backward on CTA pairs (cta_group::2), timed like
+    # the headline's backward over its ring-step launches, on its own buffers.
+    pairs_ms = None
+    if D == 128:
+        plan.set_bwd_cta_pairs(True)
+        _, wbp = plan.workspace_bytes(False, False)
+        ws_p = torch.empty(wbp, dtype=torch.uint8, device=dev)
+        dq_p, dk_p, dv_p = torch.empty_like(dq), torch.empty_like(dk), torch.empty_like(dv)
+
+        def pair_bwd(ev=None):
+            chk(lib.ra_bwd_prepare(H, P_(o), 0, P_(do), P_(lse), P_(dq_p), P_(dk_p), P_(dv_p), 0, P_(ws_p), wbp, sp))
+            if ev:
+                ev[0].record(stream)
+            for s in range(steps):
+                chk(lib.ra_bwd_ring_step(H, s, P_(q), P_(k), P_(v), P_(do), P_(dq_p), P_(dk_p), P_(dv_p), 0,
+                                         P_(ws_p), wbp, sp))
+            if ev:
+                ev[1].record(stream)
+            chk(lib.ra_bwd_finish(H, P_(dq_p), P_(dk_p), P_(dv_p), 0, P_(ws_p), wbp, sp))
+
+        for _ in range(max(1, args.warmup)):
+            pair_bwd()
+        torch.cuda.synchronize()
+        pev = [(new_event(), new_event()) for _ in range(args.steps)]
+        for it in range(args.steps):
+            pair_bwd(pev[it])
+        torch.cuda.synchronize()
+        chk(lib.ra_workspace_status(P_(ws_p), sp))
+        pairs_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in pev), dist, dev) / args.steps
+        plan.set_bwd_cta_pairs(False)
+        del ws_p, dq_p, dk_p, dv_p
+
     ff, fb = useful_flops(wl)
     ms_step = ms_total / args.steps
     value = whole_job_tflops(world, ff + fb, args.steps, ms_total)
     peak_b, peak_s, hbm, peak_kind = peaks()
     fwd_ms = sum(t_f) / args.steps
     bwd_ms = sum(t_b) / args.steps
+    cta_pairs = None if pairs_ms is None else {
+        "bwd_kernels_ms": pairs_ms, "bwd_tflops": fb / (pairs_ms * 1e-3) / 1e12,
+        "note": "the backward on CTA pairs (ra_plan_set_bwd_cta_pairs: cta_group::2 over two key tiles), timed "
+                "separately over its ring-step launches; not part of value"}
     ring_steps = {"fwd_kernels_ms": rs_kernel_ms, "fwd_tflops": ff / (rs_kernel_ms * 1e-3) / 1e12,
                   "launches": fwd_launches,
                   "note": "forward with one launch per ring step (ra_fwd_ring_steps), timed separately over "
@@ -629,7 +666,7 @@ def main():
             "bwd_tflops": fb / (bwd_ms * 1e-3) / 1e12 if bwd_ms else None,
             "useful_flops_per_step": ff + fb, "strict_bwd_flops_per_step": 0.8 * fb,
             "roofline": roof, "roofline_other_kernels": roof_other, "cpu_baseline": cpu,
-            "parity_vs_oracle": parity, "e2e": e2e, "ring_step_forward": ring_steps,
+            "parity_vs_oracle": parity, "e2e": e2e, "ring_step_forward": ring_steps, "bwd_cta_pairs": cta_pairs,
             # per step: the forward's work-list set-up and forward kernel, the
             # backward's work-list set-up and Delta preprocess, its ring steps
             # and the three gradient casts (a plan without pinned work lists

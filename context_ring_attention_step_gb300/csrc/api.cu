@@ -33,6 +33,7 @@ using ra::FwdItem;
 
 struct ra_plan {
   int32_t T = 0, num_docs = 0, Hq = 0, Hkv = 0, D = 0, causal = 1, layout = 1, steps = 0;
+  int32_t bwd_cta_pairs = 0;  // head_dim 128 backward on CTA pairs (ra_plan_set_bwd_cta_pairs)
   float scale = 0.f;
   std::vector<int32_t> cu, cp;
   std::vector<FwdItem> fwd;
@@ -105,6 +106,9 @@ int shard(int32_t L, int32_t cp, int32_t layout, int32_t r, int32_t* b, int32_t*
 
 int32_t tiles128(int32_t a, int32_t b) { return b > a ? (b - a + 127) / 128 : 0; }
 
+// The backward on CTA pairs over two key tiles (head_dim 128, when asked for).
+bool bwd_pairs(const ra_plan& P) { return P.D == 128 && P.bwd_cta_pairs != 0; }
+
 // Query rows of one forward CTA: two 128-row tiles at head_dim 64/128, one at
 // head_dim 256 (whose output accumulator alone takes half of tensor memory).
 int32_t rows_per_item(const ra_plan& P) { return P.D == 256 ? 128 : 256; }
@@ -158,15 +162,21 @@ void build_items(ra_plan& P) {
         // ---- backward: key/value shard r is held by query shard (r + s) mod cp.
         // One item per (key tile, key/value head), grouped by shard pair and
         // head: the CTAs running together then reduce into the dQ rows of one
-        // query shard and one GQA group, a working set that stays in L2.
+        // query shard and one GQA group, a working set that stays in L2.  At
+        // head_dim 128 the items come in pairs, neighbouring key tiles of one
+        // range for the two CTAs of a cluster (bwd_pair.cu): both walk the query
+        // rows the first tile meets (a superset of the second's; the rest is
+        // masked), and a range with an odd number of tiles ends in an empty one.
         const int32_t qr = (r + s) % cp;
         int32_t kb2[2], ke2[2], qb2[2], qe2[2];
         const int nk2 = shard(L, cp, P.layout, r, kb2, ke2);
         const int nq2 = shard(L, cp, P.layout, qr, qb2, qe2);
+        const bool pairs = bwd_pairs(P);
         for (int32_t g = 0; g < P.Hkv; ++g)
         for (int a = 0; a < nk2; ++a) {
-          for (int32_t k0 = base + kb2[a]; k0 < base + ke2[a]; k0 += 128) {
-            const int32_t k1 = std::min(k0 + 128, base + ke2[a]);
+          const int32_t ke = base + ke2[a];
+          for (int32_t k0 = base + kb2[a]; k0 < ke; k0 += pairs ? 256 : 128) {
+            const int32_t k1 = std::min(k0 + 128, ke);
             BwdItem it{};
             it.k0 = k0;
             it.k1 = k1;
@@ -184,6 +194,12 @@ void build_items(ra_plan& P) {
             it.tiles = tiles128(it.qb0, it.qe0) + tiles128(it.qb1, it.qe1);
             bs.push_back(it);
             br[qr].push_back(it);
+            if (pairs) {
+              it.k0 = k1;
+              it.k1 = std::min(k0 + 256, ke);
+              bs.push_back(it);
+              br[qr].push_back(it);
+            }
           }
         }
       }
@@ -509,6 +525,22 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
 }
 
 void ra_plan_destroy(ra_plan* plan) { delete plan; }
+
+ra_status ra_plan_set_bwd_cta_pairs(ra_plan* P, int32_t on) {
+  if (!P) return fail(RA_ERR_INVALID_ARG, "plan is NULL");
+  if (on != 0 && on != 1) return fail(RA_ERR_INVALID_ARG, "on must be 0 or 1 (got %d)", on);
+  if (on && P->D != 128) return fail(RA_ERR_UNSUPPORTED, "the CTA-pair backward needs head_dim 128 (got %d)", P->D);
+  if (P->bwd_cta_pairs == on) return RA_OK;
+  P->bwd_cta_pairs = on;
+  build_items(*P);  // the backward items pair up (or not); the forward lists are rebuilt unchanged
+  if (P->staged) {
+    cudaFreeHost(P->staged);
+    P->staged = nullptr;
+    P->staged_dev = nullptr;
+  }
+  stage_work_lists(*P);
+  return RA_OK;
+}
 
 ra_status ra_plan_workspace_bytes(const ra_plan* P, int32_t o_is_fp32, int32_t grads_fp32, size_t* fwd_bytes,
                                   size_t* bwd_bytes) {
@@ -840,16 +872,19 @@ static ra_status bwd_step_launch(const ra_plan* P, size_t list, int64_t first, i
   // head_dim 256: 64-row query tiles (with K and V resident, shared memory
   // holds one 64-row Q and dO tile)
   const int qrows = P->D == 256 ? 64 : 128;
-  CUtensorMap tq, tk, tv, tdo, tl, td, tdq;
+  CUtensorMap tq, tk, tv, tdo, tl, td, tdq, tq64, tdo64;
   if (!encode_thd(&tq, q, P->T, P->Hq, P->D, qrows) || !encode_thd(&tk, k, P->T, P->Hkv, P->D) ||
       !encode_thd(&tv, v, P->T, P->Hkv, P->D) || !encode_thd(&tdo, dout, P->T, P->Hq, P->D, qrows) ||
       !encode_rows(&tl, p.lse2, p.stat_pitch, P->Hq, qrows) ||
       !encode_rows(&td, p.delta, p.stat_pitch, P->Hq, qrows) || !encode_acc(&tdq, p.dq_acc, P->T, P->Hq, P->D))
     return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
-  cudaError_t e = P->D == 256 ? ra::launch_bwd_step_d256(tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
-                                                          reinterpret_cast<cudaStream_t>(stream_))
-                              : ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, tdq, p, (int)n,
-                                                    reinterpret_cast<cudaStream_t>(stream_));
+  // CTA pairs: each CTA loads 64 of a query tile's 128 rows of Q and dO for S and dP
+  if (bwd_pairs(*P) && (!encode_thd(&tq64, q, P->T, P->Hq, P->D, 64) || !encode_thd(&tdo64, dout, P->T, P->Hq, P->D, 64)))
+    return fail(RA_ERR_CUDA, "cuTensorMapEncodeTiled failed (driver entry point unavailable or bad tensor)");
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream_);
+  cudaError_t e = P->D == 256      ? ra::launch_bwd_step_d256(tq, tk, tv, tdo, tl, td, tdq, p, (int)n, st)
+                  : bwd_pairs(*P) ? ra::launch_bwd_step_pair(tq, tq64, tk, tv, tdo, tdo64, tl, td, tdq, p, (int)n, st)
+                                  : ra::launch_bwd_step(P->D, tq, tk, tv, tdo, tl, td, tdq, p, (int)n, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward step launch");
   return RA_OK;
 }

@@ -32,6 +32,7 @@
 // K-major A operand of dK = dS^T Q and the MN-major A operand of dQ = dS K.
 #include "ring_attn_internal.h"
 #include "tc.cuh"
+#include "bwd_tiles.cuh"
 
 namespace ra {
 namespace {
@@ -59,29 +60,6 @@ struct BwdCfg {
   // 4e-5 and cover every CTA of a 16-step 128K ring without a flush.
   static constexpr int kChain = 256;
 };
-
-// Query tiles of the CTA's pairs.  Tiles of a range start at the range start
-// rounded down to a multiple of 4, so the LSE/Delta slice of every tile is a
-// 16-byte aligned TMA load; columns before the range start are masked.
-struct PairList {
-  int qb0, qe0, qb1, qe1, n0, nt, G, hbase;
-  __device__ __forceinline__ int tile(int i) const { return i % nt; }
-  __device__ __forceinline__ int head(int i) const { return hbase + i / nt; }
-  __device__ __forceinline__ int start(int i) const {
-    const int t = tile(i);
-    return t < n0 ? (qb0 & ~3) + 128 * t : (qb1 & ~3) + 128 * (t - n0);
-  }
-  __device__ __forceinline__ int lo(int i) const { return tile(i) < n0 ? qb0 : qb1; }
-  __device__ __forceinline__ int end(int i) const { return tile(i) < n0 ? qe0 : qe1; }
-};
-
-__device__ __forceinline__ int ceil128(int a, int b) { return b > a ? (b - a + 127) / 128 : 0; }
-
-__device__ __forceinline__ void red_add_v4(float* addr, float a, float b, float c, float d) {
-  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(addr), "f"(a), "f"(b), "f"(c), "f"(d)
-               : "memory");
-}
-
 
 template <int D>
 __global__ void __launch_bounds__(512, 1)

@@ -83,6 +83,12 @@ cudaError_t launch_fwd_step_d256(const CUtensorMap& tq, const CUtensorMap& tk, c
                                  const FwdParams& p, int num_items, cudaStream_t stream);
 cudaError_t launch_fwd_fused_d256(const CUtensorMap& tq, const CUtensorMap& tk, const CUtensorMap& tv,
                                   const FwdParams& p, int num_items, cudaStream_t stream);
+// head_dim 128 (bwd_pair.cu): clusters of two CTAs over two key tiles; the
+// items come in pairs (num_items even), q64/dout64 with 64-row boxes.
+cudaError_t launch_bwd_step_pair(const CUtensorMap& tq, const CUtensorMap& tq64, const CUtensorMap& tk,
+                                 const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tdo64,
+                                 const CUtensorMap& tl, const CUtensorMap& td, const CUtensorMap& tdq,
+                                 const BwdParams& p, int num_items, cudaStream_t stream);
 cudaError_t launch_bwd_step(int head_dim, const CUtensorMap& tq, const CUtensorMap& tk,
                             const CUtensorMap& tv, const CUtensorMap& tdo, const CUtensorMap& tlse2,
                             const CUtensorMap& tdelta, const CUtensorMap& tdq_acc, const BwdParams& p,

@@ -54,6 +54,8 @@ def load_library(path: str | None = None):
     lib.ra_plan_workspace_bytes.restype = i32
     lib.ra_plan_stats.argtypes = [P, c.POINTER(i32), c.POINTER(i64), c.POINTER(i64), c.POINTER(i64)]
     lib.ra_plan_stats.restype = i32
+    lib.ra_plan_set_bwd_cta_pairs.argtypes = [P, i32]
+    lib.ra_plan_set_bwd_cta_pairs.restype = i32
     lib.ra_shard_token_ranges.argtypes = [P, i32, i32, c.POINTER(i32), c.POINTER(i32), c.POINTER(i32)]
     lib.ra_shard_token_ranges.restype = i32
     lib.ra_plan_work_items.argtypes = [P, i32, c.POINTER(i32), i64, c.POINTER(i64), c.POINTER(i64)]
@@ -116,7 +118,9 @@ class Plan:
     """Host-side ring plan: shards, ring pairing and GPU work items."""
 
     def __init__(self, cu_seqlens, cp_size, layout="zigzag", causal=True, num_q_heads=1,
-                 num_kv_heads=1, head_dim=128, scale=None):
+                 num_kv_heads=1, head_dim=128, scale=None, bwd_cta_pairs=False):
+        """``bwd_cta_pairs=True`` (head_dim 128) runs the backward on CTA pairs
+        (ra_plan_set_bwd_cta_pairs)."""
         lib = load_library()
         cu = [int(x) for x in (cu_seqlens.tolist() if hasattr(cu_seqlens, "tolist") else cu_seqlens)]
         self.num_docs = len(cu) - 1
@@ -136,6 +140,15 @@ class Plan:
                                   cp_all, LAYOUTS[layout] if isinstance(layout, str) else int(layout),
                                   1 if causal else 0, self.Hq, self.Hkv, self.D,
                                   float(scale) if scale else 0.0))
+        self.bwd_cta_pairs = False
+        if bwd_cta_pairs:
+            self.set_bwd_cta_pairs(True)
+
+    def set_bwd_cta_pairs(self, on=True):
+        """Backward on CTA pairs (head_dim 128) or on single CTAs; rebuilds the
+        plan's backward work lists."""
+        _check(_lib.ra_plan_set_bwd_cta_pairs(self._handle, 1 if on else 0))
+        self.bwd_cta_pairs = bool(on)
 
     def __del__(self):
         h = getattr(self, "_handle", None)

@@ -111,6 +111,23 @@ ra_status ra_plan_create(ra_plan** out, const int32_t* cu_seqlens, int32_t num_d
 void ra_plan_destroy(ra_plan* plan);
 
 /*
+ * Run the plan's backward (ra_bwd, ra_bwd_ring_step, ra_bwd_ring_step_rank) on
+ * CTA pairs: at head_dim 128 a cluster of two CTAs takes two neighbouring
+ * 128-key tiles of one key/value head and issues its matrix products as
+ * cta_group::2 tensor-core operations (M = 256 over the pair's keys for S, dP,
+ * dV, dK; dQ of a 128-row query tile reduced over all 256 keys at once).  The
+ * gradients are those of the one-CTA kernel (same formulas as ra_bwd, same
+ * accumulation order within a key tile).  on = 0 (the default) or 1.  Changing
+ * it rebuilds the plan's backward work lists (pairs of neighbouring key
+ * tiles; a range with an odd number of tiles ends in an empty one), so it is
+ * a host call to make between launches, not while work of this plan is in
+ * flight.  RA_ERR_UNSUPPORTED for head_dim != 128, RA_ERR_INVALID_ARG for a
+ * NULL plan or `on` outside {0, 1}.  This option is this library's own: the
+ * pages describe no kernel design.
+ */
+ra_status ra_plan_set_bwd_cta_pairs(ra_plan* plan, int32_t on);
+
+/*
  * Workspace sizes in bytes for ra_fwd (status header, work list and key-tile
  * table; the same for either output dtype, o_is_fp32 is accepted for
  * symmetry) and ra_bwd (given grads_fp32: bf16 gradients add their fp32

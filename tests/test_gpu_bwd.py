@@ -29,11 +29,11 @@ def ra():
     return m
 
 
-def _run(ra, wl, q, k, v, do, grads_fp32=False, cp=None, layout=None, o_fp32=False):
+def _run(ra, wl, q, k, v, do, grads_fp32=False, cp=None, layout=None, o_fp32=False, pairs=False):
     cps = list(wl.cp_per_doc) if cp is None else cp
     lay = layout or wl.layout
     qd, kd, vd, dod = q.cuda(), k.cuda(), v.cuda(), do.cuda()
-    plan = ra.Plan(wl.cu_seqlens, cps, lay, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan = ra.Plan(wl.cu_seqlens, cps, lay, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale, bwd_cta_pairs=pairs)
     o, lse = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, lay, wl.causal, wl.softmax_scale,
                               o_fp32=o_fp32, plan=plan, check=True)
     dq, dk, dv = ra.ring_attn_bwd(qd, kd, vd, o, dod, lse, wl.cu_seqlens, cps, lay, wl.causal,
@@ -42,11 +42,11 @@ def _run(ra, wl, q, k, v, do, grads_fp32=False, cp=None, layout=None, o_fp32=Fal
     return tuple(x.float().cpu().numpy() for x in (dq, dk, dv))
 
 
-def _check_vs_oracle(ra, wl):
+def _check_vs_oracle(ra, wl, pairs=False):
     q, k, v, do = draw_qkvdo(wl)
     rq, rk, rv, _, _ = A.attention_bwd(q, k, v, do, wl.cu_seqlens, wl.causal, wl.softmax_scale)
     for fp32 in (True, False):
-        grads = _run(ra, wl, q, k, v, do, grads_fp32=fp32)
+        grads = _run(ra, wl, q, k, v, do, grads_fp32=fp32, pairs=pairs)
         for name, x, ref in zip(("dq", "dk", "dv"), grads, (rq, rk, rv)):
             assert np.isfinite(x).all(), name
             bound = G_TOL if fp32 else G_TOL + np.abs(ref) * 2.0 ** -9
@@ -69,6 +69,26 @@ def test_multi_tile_ragged_gqa(ra, layout, causal):
 def test_varlen_docs_per_doc_cp(ra, d):
     wl = custom([300, 1, 5, 777, 129, 64], 4, 1, d, [3, 1, 2, 5, 8, 1], "zigzag", True, seed=22, name="varlen")
     _check_vs_oracle(ra, wl)
+
+
+@pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
+@pytest.mark.parametrize("causal", [True, False])
+def test_cta_pair_backward_ragged_gqa(ra, layout, causal):
+    """The CTA-pair backward (head_dim 128): key tiles in pairs, one of them
+    ragged or empty at every range end, GQA, multi-document."""
+    wl = custom([1500, 77, 300], 4, 2, 128, [3, 1, 2], layout, causal, seed=26, name="pairs_bwd")
+    _check_vs_oracle(ra, wl, pairs=True)
+
+
+def test_cta_pair_backward_equals_single_cta(ra):
+    """Same gradients from the CTA-pair backward as from the one-CTA kernel,
+    within fp32 accumulation-order differences (fp32 gradients)."""
+    wl = custom([2500], 8, 2, 128, 4, "zigzag", True, seed=27, name="pairs_vs_single")
+    q, k, v, do = draw_qkvdo(wl)
+    one = _run(ra, wl, q, k, v, do, grads_fp32=True)
+    two = _run(ra, wl, q, k, v, do, grads_fp32=True, pairs=True)
+    for name, a, b in zip(("dq", "dk", "dv"), one, two):
+        assert np.abs(a - b).max() <= RING_TOL, (name, np.abs(a - b).max())
 
 
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])

@@ -54,10 +54,11 @@ def _group_reference(wl, q, k, v, do, g):
     return {"o": o, "lse": lse, "dq": dq, "dk": dk[:, 0], "dv": dv[:, 0]}
 
 
-def _gpu_group(ra, wl, qd, kd, vd, dod, g, o_fp32, grads_fp32, fused):
+def _gpu_group(ra, wl, qd, kd, vd, dod, g, o_fp32, grads_fp32, fused, pairs=False):
     G = wl.Hq // wl.Hkv
     cps = list(wl.cp_per_doc)
-    plan = ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan = ra.Plan(wl.cu_seqlens, cps, wl.layout, wl.causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale,
+                   bwd_cta_pairs=pairs)
     o, lse = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, wl.layout, wl.causal, wl.softmax_scale,
                               o_fp32=o_fp32, plan=plan, check=True, fused=fused)
     dq, dk, dv = ra.ring_attn_bwd(qd, kd, vd, o, dod, lse, wl.cu_seqlens, cps, wl.layout, wl.causal,
@@ -102,6 +103,20 @@ def test_llama_32k_full_kv_group(ra):
     _full_group_check(ra, workload("llama3_8b_32k"))
 
 
+@pytest.mark.parametrize("name", ["llama3_8b_32k", "varlen_65k"])
+def test_cta_pair_backward_full_kv_group(ra, name):
+    """The CTA-pair backward in the bench's launch configuration (bf16 outputs)
+    and with fp32 gradients, one whole KV-head group element by element."""
+    wl = workload(name)
+    q, k, v, do = draw_qkvdo(wl)
+    ref = _group_reference(wl, q, k, v, do, 0)
+    qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
+    _compare(wl.name + " pairs bf16", _gpu_group(ra, wl, qd, kd, vd, dod, 0, False, False, None, True), ref, True,
+             True)
+    _compare(wl.name + " pairs fp32", _gpu_group(ra, wl, qd, kd, vd, dod, 0, True, True, None, True), ref, False,
+             False)
+
+
 def test_varlen_65k_full_kv_group(ra):
     _full_group_check(ra, workload("varlen_65k"))
 
@@ -123,3 +138,6 @@ def test_dkdv_chain_flush_cp1(ra, d, causal, L):
              _gpu_group(ra, wl, qd, kd, vd, dod, 0, True, True, None), ref, False, False)
     _compare("chain flush d=%d causal=%s bf16" % (d, causal),
              _gpu_group(ra, wl, qd, kd, vd, dod, 0, False, False, None), ref, True, True)
+    if d == 128:  # the CTA-pair backward flushes its own chains
+        _compare("chain flush d=%d causal=%s pairs fp32" % (d, causal),
+                 _gpu_group(ra, wl, qd, kd, vd, dod, 0, True, True, None, True), ref, False, False)

@@ -75,23 +75,32 @@ def _expand_fwd(items, off, causal):
     return cover
 
 
-def _expand_bwd(items, off, causal, head=0):
-    """Pairs covered by the backward items of one key/value head."""
+def _expand_bwd(items, off, causal, head=0, pairs=False):
+    """Pairs covered by the backward items of one key/value head.  With
+    `pairs` (head_dim 128: CTA pairs over two key tiles) items come two by two,
+    neighbouring key tiles with the same query ranges, the second possibly
+    empty."""
     cover = {}
     for s in range(len(off) - 1):
-        pairs = []
-        for it in items[off[s]:off[s + 1]]:
+        step = items[off[s]:off[s + 1]]
+        if pairs:
+            assert len(step) % 2 == 0
+            for a, b in zip(step[0::2], step[1::2]):
+                assert a[2:] == b[2:] and b[0] == a[1] and b[1] - b[0] <= 128
+                assert a[1] - a[0] == 128 or b[1] == b[0]
+        pairs_ = []
+        for n, it in enumerate(step):
             k0, k1, qb0, qe0, qb1, qe1, flags, tiles = it
             assert (flags & 1) == (s == 0)
             if flags >> 8 != head:
                 continue
-            assert k1 - k0 <= 128 and k1 > k0
+            assert k1 - k0 <= 128 and (k1 > k0 or (pairs and n % 2 == 1))
             for k in range(k0, k1):
                 for qb, qe in ((qb0, qe0), (qb1, qe1)):
                     for q in range(qb, qe):
                         if not causal or k <= q:
-                            pairs.append((q, k))
-        cover[s] = pairs
+                            pairs_.append((q, k))
+        cover[s] = pairs_
     return cover
 
 
@@ -111,12 +120,16 @@ def _expected(wl, causal):
 
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("causal", [True, False])
-@pytest.mark.parametrize("lengths,cp", [([512], 4), ([700, 3, 1, 260], [4, 2, 1, 3]), ([130, 9], 8)])
-def test_work_items_cover_each_visible_pair_once(ra, layout, causal, lengths, cp):
-    wl = custom(lengths, 2, 2, 64, cp, layout, causal)
-    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), layout, causal, 2, 2, 64)
+@pytest.mark.parametrize("lengths,cp", [([512], 4), ([700, 3, 1, 260], [4, 2, 1, 3]), ([130, 9], 8),
+                                        ([600, 300], [1, 1])])
+@pytest.mark.parametrize("head_dim", [64, 128])  # 128: with the CTA-pair backward
+def test_work_items_cover_each_visible_pair_once(ra, layout, causal, lengths, cp, head_dim):
+    wl = custom(lengths, 2, 2, head_dim, cp, layout, causal)
+    paired = head_dim == 128
+    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), layout, causal, 2, 2, head_dim, bwd_cta_pairs=paired)
     want = _expected(wl, causal)
-    expanders = [("fwd", _expand_fwd)] + [("bwd", lambda i, o, c, h=h: _expand_bwd(i, o, c, h)) for h in range(2)]
+    expanders = [("fwd", _expand_fwd)] + [("bwd", lambda i, o, c, h=h: _expand_bwd(i, o, c, h, paired))
+                                          for h in range(2)]
     for which, expand in expanders:
         items, off = plan.work_items(which)
         got = expand(items, off, causal)
@@ -306,3 +319,20 @@ def test_rank_work_lists_partition_each_step(ra, layout, lengths, cp):
                         assert qs <= rows_r
                         d = next(i for i in range(len(lengths)) if cu[i] <= it[0] < cu[i + 1])
                         assert set(range(it[0], it[1])) <= shard_rows((r - s) % cps[d]) or cps[d] <= s
+
+
+def test_bwd_cta_pairs_option(ra):
+    """The CTA-pair backward: head_dim 128 only; switching it rebuilds the
+    backward items (pairs of neighbouring key tiles) and back again."""
+    wl = custom([700, 300], 4, 2, 128, [2, 1], "zigzag")
+    plan = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), "zigzag", True, 4, 2, 128)
+    single, off1 = plan.work_items("bwd")
+    plan.set_bwd_cta_pairs(True)
+    paired, off2 = plan.work_items("bwd")
+    assert len(paired) % 2 == 0 and len(paired) >= len(single) and paired != single
+    assert all(b[1] - b[0] <= 128 for b in paired)
+    plan.set_bwd_cta_pairs(False)
+    assert plan.work_items("bwd") == (single, off1)
+    p64 = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), "zigzag", True, 4, 2, 64)
+    with pytest.raises(ra.RingAttnError):
+        p64.set_bwd_cta_pairs(True)
