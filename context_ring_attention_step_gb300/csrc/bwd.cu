@@ -42,12 +42,17 @@ struct BwdCfg {
   static constexpr int kTile = 128 * D * 2;   // one 128-row bf16 tile
   static constexpr int kK = 0;
   static constexpr int kV = kTile;
-  static constexpr int kQ0 = 2 * kTile;       // two Q stages
-  static constexpr int kDO = 4 * kTile;       // one dO buffer
-  static constexpr int kDS = 5 * kTile;       // dS^T, 128 x 128 bf16
-  static constexpr int kStg = kDS + 32768;    // dQ staging, 128 rows x 64 fp32
-  static constexpr int kStat = kStg + 32768;  // per Q stage: lse2[128], delta[128]
-  static constexpr int kBar = kStat + 2 * 1024;
+  // Q (with its LSE/Delta slices) and dO rings: at head_dim 64 a pair is
+  // shorter than a tile's load latency, and 16 KB tiles leave room for more
+  // stages
+  static constexpr int kNQ = D == 64 ? 4 : 2;
+  static constexpr int kNDO = D == 64 ? 2 : 1;
+  static constexpr int kQ0 = 2 * kTile;                 // Q stages
+  static constexpr int kDO = kQ0 + kNQ * kTile;         // dO stages
+  static constexpr int kDS = kDO + kNDO * kTile;        // dS^T, 128 x 128 bf16
+  static constexpr int kStg = kDS + 32768;              // dQ staging, 128 rows x 64 fp32
+  static constexpr int kStat = kStg + 32768;            // per Q stage: lse2[128], delta[128]
+  static constexpr int kBar = kStat + kNQ * 1024;
   static constexpr int kSmem = kBar + 256;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(128, 128, false, false);
   static constexpr uint32_t kIdescG = idesc_bf16_f32(128, D, false, true);   // dV, dK: A tmem, B MN-major
@@ -80,10 +85,10 @@ __global__ void __launch_bounds__(512, 1)
   float* stat = reinterpret_cast<float*>(smem + C::kStat);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kBar);
   const uint32_t b_kv = smem_u32(bars + 0);
-  const uint32_t b_qfull = smem_u32(bars + 1);   // [2] Q_i + LSE/Delta landed
-  const uint32_t b_qempty = smem_u32(bars + 3);  // [2] Q stage released (after dK_i)
-  const uint32_t b_dofull = smem_u32(bars + 5);  // dO_i landed
-  const uint32_t b_doempty = smem_u32(bars + 6); // dO released (after dV_i)
+  const uint32_t b_qfull = smem_u32(bars + 17);                          // [kNQ] Q_i + LSE/Delta landed
+  const uint32_t b_qempty = smem_u32(bars + 17 + C::kNQ);               // [kNQ] Q stage released (after dK_i)
+  const uint32_t b_dofull = smem_u32(bars + 17 + 2 * C::kNQ);           // [kNDO] dO_i landed
+  const uint32_t b_doempty = smem_u32(bars + 17 + 2 * C::kNQ + C::kNDO); // [kNDO] dO released (after dV_i)
   const uint32_t b_s = smem_u32(bars + 7);       // S^T_i in TMEM
   const uint32_t b_dp = smem_u32(bars + 8);      // dP^T_i in TMEM
   const uint32_t b_pr = smem_u32(bars + 9);      // dS^T_i written to shared memory
@@ -109,9 +114,8 @@ __global__ void __launch_bounds__(512, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(b_kv, 1);
-    mbar_init(b_qfull, 1); mbar_init(b_qfull + 8, 1);
-    mbar_init(b_qempty, 1); mbar_init(b_qempty + 8, 1);
-    mbar_init(b_dofull, 1); mbar_init(b_doempty, 1);
+    for (int x = 0; x < C::kNQ; ++x) { mbar_init(b_qfull + 8 * x, 1); mbar_init(b_qempty + 8 * x, 1); }
+    for (int x = 0; x < C::kNDO; ++x) { mbar_init(b_dofull + 8 * x, 1); mbar_init(b_doempty + 8 * x, 1); }
     mbar_init(b_s, 1); mbar_init(b_dp, 1);
     mbar_init(b_pr, 8);    // arrivals are one per warp (8 compute warps): the shared-memory
                            // unit takes an mbarrier's arrivals one at a time
@@ -156,9 +160,9 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_3d(sV + hf * 16384, &tmV, b_kv, 64 * hf, g, it.k0);
       }
       for (int i = 0; i < npairs; ++i) {
-        const int st = i & 1;
+        const int st = i % C::kNQ, sd = i % C::kNDO;
         const int h = pl.head(i), q0 = pl.start(i);
-        if (!mbar_wait(b_qempty + 8 * st, ((i >> 1) & 1) ^ 1, ab, 201)) { ok = false; break; }
+        if (!mbar_wait(b_qempty + 8 * st, ((i / C::kNQ) & 1) ^ 1, ab, 201)) { ok = false; break; }
         const uint32_t sq = sQ + st * C::kTile;
         const uint32_t sl = smem_u32(stat + st * 256);
         mbar_expect_tx(b_qfull + 8 * st, C::kTile + 2 * 512);
@@ -167,9 +171,10 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_2d(sl, &tmL, b_qfull + 8 * st, q0, h);
         tma_load_2d(sl + 512, &tmD, b_qfull + 8 * st, q0, h);
         ++issued_q;
-        if (!mbar_wait(b_doempty, (i & 1) ^ 1, ab, 206)) { ok = false; break; }
-        mbar_expect_tx(b_dofull, C::kTile);
-        for (int hf = 0; hf < D / 64; ++hf) tma_load_3d(sDO + hf * 16384, &tmDO, b_dofull, 64 * hf, h, q0);
+        if (!mbar_wait(b_doempty + 8 * sd, ((i / C::kNDO) & 1) ^ 1, ab, 206)) { ok = false; break; }
+        mbar_expect_tx(b_dofull + 8 * sd, C::kTile);
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_3d(sDO + sd * C::kTile + hf * 16384, &tmDO, b_dofull + 8 * sd, 64 * hf, h, q0);
         ++issued_do;
       }
       {
@@ -187,9 +192,10 @@ __global__ void __launch_bounds__(512, 1)
       }
       if (!ok) {  // drain this CTA's copies still in flight
         mbar_wait_drain(b_kv, 0);
-        for (int i = issued_q > 2 ? issued_q - 2 : 0; i < issued_q; ++i)
-          mbar_wait_drain(b_qfull + 8 * (i & 1), (i >> 1) & 1);
-        if (issued_do > 0) mbar_wait_drain(b_dofull, (issued_do - 1) & 1);
+        for (int i = issued_q > C::kNQ ? issued_q - C::kNQ : 0; i < issued_q; ++i)
+          mbar_wait_drain(b_qfull + 8 * (i % C::kNQ), (i / C::kNQ) & 1);
+        for (int i = issued_do > C::kNDO ? issued_do - C::kNDO : 0; i < issued_do; ++i)
+          mbar_wait_drain(b_dofull + 8 * (i % C::kNDO), (i / C::kNDO) & 1);
       }
     } else if (warp == 1 && lane == 0) {
       // ---------------------------------------------------------- MMA issuer
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(512, 1)
       const uint64_t d0 = sdesc_sw128(s0, 0, 1024);
       auto issue_s = [&](int i) {  // S^T_i = K Q_i^T
         const uint64_t dk = opaque(d0);
-        const uint64_t dq = sdesc_at(dk, (uint32_t)(i & 1) * C::kTile, 0);
+        const uint64_t dq = sdesc_at(dk, (uint32_t)(i % C::kNQ) * C::kTile, 0);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
@@ -208,12 +214,13 @@ __global__ void __launch_bounds__(512, 1)
         }
         umma_commit(b_s);
       };
-      auto issue_dp = [&]() {  // dP^T = V dO^T
+      auto issue_dp = [&](int i) {  // dP^T_i = V dO_i^T
         const uint64_t dv = opaque(d0);
+        const uint64_t dd = sdesc_at(dv, (uint32_t)(i % C::kNDO) * C::kTile, 0);  // dO_i's stage
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-          umma_ss(tmem + C::tP, sdesc_at(dv, C::kV + off, 16), sdesc_at(dv, C::kDO + off, 16), C::kIdescS, kk > 0);
+          umma_ss(tmem + C::tP, sdesc_at(dv, C::kV + off, 16), sdesc_at(dd, C::kDO + off, 16), C::kIdescS, kk > 0);
         }
         umma_commit(b_dp);
       };
@@ -223,14 +230,15 @@ __global__ void __launch_bounds__(512, 1)
         if (ok) {
           tc_fence_after();
           issue_s(0);
-          issue_dp();
+          issue_dp(0);
         }
       }
       for (int i = 0; i < npairs && ok; ++i) {
-        const int st = i & 1;
+        const int st = i % C::kNQ, sd = i % C::kNDO;
         const uint32_t pi = i & 1;
         const uint64_t db = opaque(d0);
         const uint64_t dq = sdesc_at(db, (uint32_t)st * C::kTile, 0);  // this pair's Q stage
+        const uint64_t dd = sdesc_at(db, (uint32_t)sd * C::kTile, 0);  // this pair's dO stage
         // dV += P^T dO once P_i is packed (A from tensor memory: query columns
         // 0-63 in columns [0,32) of the S region, 64-127 in [64,96); B MN-major)
         if (!mbar_wait(b_p, pi, ab, 205)) { ok = false; break; }
@@ -240,12 +248,12 @@ __global__ void __launch_bounds__(512, 1)
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(db, C::kDO + kk * 2048, 16384),
+          umma_ts(tmem + C::tdV, tmem + C::tS + (kk >> 2) * 64 + (kk & 3) * 8, sdesc_at(dd, C::kDO + kk * 2048, 16384),
                   C::kIdescG, (i % C::kChain > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(b_doempty);
+        umma_commit(b_doempty + 8 * sd);
         // S_{i+1} right behind dV_i, the last reader of P_i in the S region
         if (i + 1 < npairs) {
-          if (!mbar_wait(b_qfull + 8 * (st ^ 1), ((i + 1) >> 1) & 1, ab, 203)) { ok = false; break; }
+          if (!mbar_wait(b_qfull + 8 * ((i + 1) % C::kNQ), ((i + 1) / C::kNQ) & 1, ab, 203)) { ok = false; break; }
           tc_fence_after();
           issue_s(i + 1);
         }
@@ -267,9 +275,9 @@ __global__ void __launch_bounds__(512, 1)
         // dP_{i+1} once dQ_i has left the region and dO_{i+1} has landed
         if (i + 1 < npairs) {
           if (!mbar_wait(b_dqf, pi, ab, 204)) { ok = false; break; }
-          if (!mbar_wait(b_dofull, pi ^ 1, ab, 207)) { ok = false; break; }
+          if (!mbar_wait(b_dofull + 8 * ((i + 1) % C::kNDO), ((i + 1) / C::kNDO) & 1, ab, 207)) { ok = false; break; }
           tc_fence_after();
-          issue_dp();
+          issue_dp(i + 1);
         }
       }
       if (!ok) {  // let issued MMAs finish before tensor memory is released
@@ -339,7 +347,7 @@ __global__ void __launch_bounds__(512, 1)
       bool need_mask;
       int cmin, cmax;
       vis(i, need_mask, cmin, cmax);
-      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i & 1) * 256);
+      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i % C::kNQ) * 256);
       uint32_t r[2][32];
       tmem_ld32(tS + 64 * wg, r[0]);
       tmem_ld32(tS + 64 * wg + 32, r[1]);
@@ -380,7 +388,7 @@ __global__ void __launch_bounds__(512, 1)
     auto ds_phase = [&](int i) -> bool {
       if (!wait_warp(b_dp, i & 1, 211)) return false;
       tc_fence_after();
-      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i & 1) * 256);
+      const float4* sl4 = reinterpret_cast<const float4*>(stat + (i % C::kNQ) * 256);
       uint32_t r[2][32];
       tmem_ld32(tP + 64 * wg, r[0]);
       tmem_ld32(tP + 64 * wg + 32, r[1]);
