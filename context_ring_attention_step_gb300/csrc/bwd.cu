@@ -350,13 +350,16 @@ __global__ void __launch_bounds__(512, 1)
       const float4* sl4 = reinterpret_cast<const float4*>(stat + (i % C::kNQ) * 256);
       uint32_t r[2][32];
       tmem_ld32(tS + 64 * wg, r[0]);
-      tmem_ld32(tS + 64 * wg + 32, r[1]);
       tmem_ld_wait();
       reg_fence32(r[0]);
-      reg_fence32(r[1]);
+      tmem_ld32(tS + 64 * wg + 32, r[1]);  // in flight while the first 32 columns are computed
       uint32_t w0[16], w1[16];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
+        if (c == 1) {
+          tmem_ld_wait();
+          reg_fence32(r[1]);
+        }
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 64 * wg + 32 * c + 2 * x;
@@ -391,13 +394,16 @@ __global__ void __launch_bounds__(512, 1)
       const float4* sl4 = reinterpret_cast<const float4*>(stat + (i % C::kNQ) * 256);
       uint32_t r[2][32];
       tmem_ld32(tP + 64 * wg, r[0]);
-      tmem_ld32(tP + 64 * wg + 32, r[1]);
       tmem_ld_wait();
       reg_fence32(r[0]);
-      reg_fence32(r[1]);
+      tmem_ld32(tP + 64 * wg + 32, r[1]);  // in flight while the first 32 columns are computed
       uint32_t w[2][16];
 #pragma unroll
       for (int c = 0; c < 2; ++c) {
+        if (c == 1) {
+          tmem_ld_wait();
+          reg_fence32(r[1]);
+        }
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 64 * wg + 32 * c + 2 * x;
