@@ -62,14 +62,24 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(src):
+    """C++ source without comments and blank lines (an edit to a comment does
+    not change the kernel)."""
+    import re
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
 def kernel_source_hash(kernel):
-    """sha256 (first 16 hex digits) of the sources a kernel is built from."""
+    """sha256 (first 16 hex digits) of the code a kernel is built from
+    (comments and blank lines removed)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "context_ring_attention_step_gb300", "csrc")
     for f in KERNEL_SOURCES[kernel]:
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            h.update(strip_comments(fh.read()).encode())
     return h.hexdigest()[:16]
 
 

@@ -12,7 +12,8 @@
 //
 // Warp roles (512 threads):
 //   warp 0       producer: K, V once; then Q_i with its LSE/Delta slices into a
-//                two-stage ring, and dO_i into a single buffer
+//                ring of kNQ stages and dO_i into a ring of kNDO (2 and 1 at
+//                head_dim 128, 4 and 2 at head_dim 64)
 //   warp 1       TMEM owner + single-thread UMMA issuer, per pair i:
 //                  [P_i written] dV_i, S_{i+1} | [dS_i written] dQ_i, dK_i |
 //                  [dQ_i read out] dP_{i+1}
