@@ -336,3 +336,15 @@ def test_bwd_cta_pairs_option(ra):
     p64 = ra.Plan(wl.cu_seqlens, list(wl.cp_per_doc), "zigzag", True, 4, 2, 64)
     with pytest.raises(ra.RingAttnError):
         p64.set_bwd_cta_pairs(True)
+
+
+def test_kernel_source_hash_ignores_comments_only():
+    """The recorded DRAM traffic is tied to the kernel's code: comments and
+    blank lines do not change the hash, code does."""
+    import bench
+    a = "// header\nint f(int x) {  // add one\n  /* block\n     comment */ return x + 1;\n}\n"
+    b = "int f(int x) {\n\n  return x + 1;   // other words\n}\n"
+    c = "int f(int x) {\n  return x + 2;\n}\n"
+    assert bench.strip_comments(a) == bench.strip_comments(b)
+    assert bench.strip_comments(a) != bench.strip_comments(c)
+    assert len(bench.kernel_source_hash("ring_bwd_step_kernel")) == 16
