@@ -63,17 +63,17 @@ KERNEL_SOURCES = {
 
 
 def strip_comments(src):
-    """C++ source without comments and blank lines (an edit to a comment does
-    not change the kernel)."""
+    """C++ source without comments, blank lines and runs of whitespace (an
+    edit to a comment or to spacing does not change the kernel)."""
     import re
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     src = re.sub(r"//[^\n]*", "", src)
-    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+    return "\n".join(" ".join(line.split()) for line in src.splitlines() if line.strip())
 
 
 def kernel_source_hash(kernel):
     """sha256 (first 16 hex digits) of the code a kernel is built from
-    (comments and blank lines removed)."""
+    (comments, blank lines and spacing removed)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "context_ring_attention_step_gb300", "csrc")
