@@ -32,6 +32,10 @@ per chunk of a shard per document) copied into the receiving rank's own
 memory: no kernel reads another GPU's memory.  The ring needs one ring size
 for every document, equal to the number of ranks.
 
+`AllGatherDriver` is the other variant the Accelerate guide describes ("all-to-all
+vs all-gather"): all key/value shards gathered once up front, the steps run
+without exchange, and the dK/dV partials summed onto their owners at the end.
+
 The exchange uses torch.distributed point-to-point calls (NCCL between GPUs,
 gloo on CPU for the tests); the compute of each step is an object with
 fwd_begin / fwd_step(s) / fwd_end and bwd_begin / bwd_step(s) / bwd_end.
@@ -119,6 +123,72 @@ class RingDriver:
         compute.bwd_end()
 
 
+class AllGatherDriver(RingDriver):
+    """The all-gather variant of the same schedule (Accelerate guide,
+    "all-to-all vs all-gather"): every rank gathers every key/value shard once,
+    before its first step, and then runs its cp ring steps with no exchange in
+    between; in the backward each key/value shard's partial dK, dV are summed
+    onto the shard's owner after the last step (one reduction per shard).  It
+    hides no transfer behind compute and holds all of K and V on every rank,
+    against the ring's one shard in flight; it needs no step-by-step
+    choreography.  Same compute interface, same results as RingDriver."""
+
+    def _sizes(self):
+        return [sum(e - b for b, e in self.ranges[j]) for j in range(self.world)]
+
+    def _pack(self, t, shard):
+        """The rows of `shard` (all its ranges, in order) as one contiguous copy."""
+        rows = [t[b:e] for b, e in self.ranges[shard]]
+        return torch.cat(rows) if rows else t[:0].clone()
+
+    def _unpack(self, t, shard, buf):
+        o = 0
+        for b, e in self.ranges[shard]:
+            t[b:e].copy_(buf[o:o + e - b])
+            o += e - b
+
+    def gather(self, tensors):
+        """Every shard's rows of each tensor onto every rank: one all_gather
+        per tensor of the packed shard rows, padded to the largest shard."""
+        n = self._sizes()
+        m = max(n)
+        for t in tensors:
+            mine = t.new_zeros((m,) + tuple(t.shape[1:]))
+            mine[:n[self.rank]] = self._pack(t, self.rank)
+            parts = [t.new_empty((m,) + tuple(t.shape[1:])) for _ in range(self.world)]
+            dist.all_gather(parts, mine, group=self.group)
+            for j in range(self.world):
+                if j != self.rank:
+                    self._unpack(t, j, parts[j][:n[j]])
+
+    def forward(self, compute, k, v):
+        """Run the forward: gather K, V, then every ring step locally."""
+        self.gather((k, v))
+        compute.fwd_begin()
+        for s in range(self.world):
+            compute.fwd_step(s)
+        compute.fwd_end()
+
+    def backward(self, compute, k, v, dk, dv):
+        """Run the backward: gather K, V, every ring step locally (the partial
+        dK, dV of every shard accumulate in this rank's full-length dk, dv),
+        then sum each shard's partials onto its owner."""
+        self.gather((k, v))
+        compute.bwd_begin()
+        for s in range(self.world):
+            compute.bwd_step(s)
+        for t in (dk, dv):
+            for j in range(self.world):
+                part = self._pack(t, j)
+                dist.reduce(part, dst=j, group=self.group)
+                if j == self.rank:
+                    self._unpack(t, j, part)
+        compute.bwd_end()
+
+
+DRIVERS = {"ring": RingDriver, "allgather": AllGatherDriver}
+
+
 class RankCompute:
     """One rank's ring steps through the library's per-rank calls: every step
     is one kernel launch over the work items of query shard `rank`.  Outputs:
@@ -179,25 +249,26 @@ class RankCompute:
         pass  # the gradients are the fp32 accumulators
 
 
-def ring_attn_fwd_rank(q, k, v, plan, rank, world, group=None, o_fp32=False, check=False):
+def ring_attn_fwd_rank(q, k, v, plan, rank, world, group=None, o_fp32=False, check=False, variant="ring"):
     """Forward of one rank of a multi-GPU ring: returns (o, lse, compute),
     with the rows of shard `rank` valid in o and lse.  q, k, v: full-length
     [T, H, d] bf16 buffers on this rank's GPU holding its own shard's rows and
     finite values (zeros) elsewhere (k and v receive the other shards' rows).
-    Keep `compute` for the backward."""
+    variant: "ring" (neighbour exchange overlapped with each step) or
+    "allgather" (all shards gathered first).  Keep `compute` for the backward."""
     comp = RankCompute(plan, rank, q, k, v, o_fp32)
-    RingDriver(plan, rank, world, group).forward(comp, k, v)
+    DRIVERS[variant](plan, rank, world, group).forward(comp, k, v)
     if check:
         _ra._check(_ra.workspace_status(comp.ws_f))
     return comp.o, comp.lse, comp
 
 
-def ring_attn_bwd_rank(compute, do, plan, rank, world, group=None, check=False):
+def ring_attn_bwd_rank(compute, do, plan, rank, world, group=None, check=False, variant="ring"):
     """Backward of one rank after ring_attn_fwd_rank: returns fp32 (dq, dk, dv)
     with the rows of shard `rank` complete.  do: full-length [T, Hq, d] bf16
     with this rank's rows and finite values (zeros) elsewhere."""
     compute.do = do
-    RingDriver(plan, rank, world, group).backward(compute, compute.k, compute.v, compute.dk, compute.dv)
+    DRIVERS[variant](plan, rank, world, group).backward(compute, compute.k, compute.v, compute.dk, compute.dv)
     if check:
         _ra._check(_ra.workspace_status(compute.ws_b))
     return compute.dq, compute.dk, compute.dv

@@ -1,4 +1,5 @@
-"""The multi-GPU ring schedule (ring_driver.RingDriver) on CPU: gloo ranks,
+"""The multi-GPU ring schedules (ring_driver.RingDriver, and its all-gather
+variant AllGatherDriver) on CPU: gloo ranks,
 world size 2 and 4, each rank computing its ring steps with the fp64 oracle's
 per-shard-pair partials (oracle/ring.py) on its own full-length buffers.
 
@@ -94,21 +95,31 @@ class _OracleCompute:
         pass
 
 
-def _worker(rank, world, port, case, out):
+def _worker(rank, world, port, case, out, kind="ring"):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
     import datetime
     dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=60))
     try:
         import context_ring_attention_step_gb300 as ra
-        from context_ring_attention_step_gb300.ring_driver import RingDriver
+        from context_ring_attention_step_gb300.ring_driver import DRIVERS, RingDriver
         from workloads import custom, draw_qkvdo
         lengths, Hq, Hkv, d, layout, causal, planted = case
-        if planted:  # a ring turning the wrong way must be caught
+        if planted and kind == "ring":  # a ring turning the wrong way must be caught
             RingDriver.source = lambda self, s: (self.rank + s) % self.world
+        if planted and kind == "allgather":  # gradients left unsummed must be caught
+            from context_ring_attention_step_gb300.ring_driver import AllGatherDriver
+
+            def no_reduce(self, c, kk, vv, dk, dv):
+                self.gather((kk, vv))
+                c.bwd_begin()
+                for st in range(self.world):
+                    c.bwd_step(st)
+                c.bwd_end()
+            AllGatherDriver.backward = no_reduce
         wl = custom(lengths, Hq, Hkv, d, world, layout, causal, seed=71)
         q, k, v, do = (x.double().numpy() for x in draw_qkvdo(wl))
         plan = ra.Plan(wl.cu_seqlens, [world] * wl.num_docs, layout, causal, Hq, Hkv, d)
-        drv = RingDriver(plan, rank, world)
+        drv = DRIVERS[kind](plan, rank, world)
         own = np.concatenate([np.arange(b, e) for b, e in drv.ranges[rank]]).astype(np.int64) \
             if drv.ranges[rank] else np.zeros(0, np.int64)
         # this rank's buffers: its own shard's rows, NaN elsewhere until they arrive
@@ -128,10 +139,10 @@ def _worker(rank, world, port, case, out):
         dist.destroy_process_group()
 
 
-def _run(world, case):
+def _run(world, case, kind="ring"):
     mgr = mp.Manager()
     out = mgr.dict()
-    mp.spawn(_worker, args=(world, _free_port(), case, out), nprocs=world, join=True)
+    mp.spawn(_worker, args=(world, _free_port(), case, out, kind), nprocs=world, join=True)
     return dict(out)
 
 
@@ -142,12 +153,14 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("kind", ["ring", "allgather"])
 @pytest.mark.parametrize("world,case", CASES)
-def test_ring_driver_matches_oracle(world, case):
+def test_ring_driver_matches_oracle(world, case, kind):
+    """Both schedules: the neighbour ring and the all-gather variant."""
     from oracle import attention as A
     from workloads import custom, draw_qkvdo
     lengths, Hq, Hkv, d, layout, causal = case
-    res = _run(world, case + (False,))
+    res = _run(world, case + (False,), kind)
     wl = custom(lengths, Hq, Hkv, d, world, layout, causal, seed=71)
     q, k, v, do = draw_qkvdo(wl)
     rdq, rdk, rdv, ro, rl = A.attention_bwd(q, k, v, do, wl.cu_seqlens, causal, wl.softmax_scale)
@@ -191,3 +204,18 @@ def test_ring_driver_requires_cp_equal_to_world():
         RingDriver(plan, 0, 4)
     with pytest.raises(ValueError):
         RingDriver(ra.Plan([0, 100], 4, "zigzag", True, 2, 1, 64), 4, 4)
+
+
+def test_allgather_driver_catches_unsummed_gradients():
+    """Without the per-shard reduction each owner keeps only its own query
+    shard's contribution to dK, dV: the comparison must fail."""
+    world, case = CASES[1]
+    res = _run(world, case + (True,), "allgather")
+    from oracle import attention as A
+    from workloads import custom, draw_qkvdo
+    lengths, Hq, Hkv, d, layout, causal = case
+    wl = custom(lengths, Hq, Hkv, d, world, layout, causal, seed=71)
+    q, k, v, do = draw_qkvdo(wl)
+    _, rdk, _, _, _ = A.attention_bwd(q, k, v, do, wl.cu_seqlens, causal, wl.softmax_scale)
+    bad = [np.abs(res[r][4] - rdk[res[r][0]]).max() > 1e-9 for r in range(world)]
+    assert any(bad)
