@@ -106,3 +106,52 @@ def test_rank_steps_emulated_ring(ra, layout, causal):
     assert np.abs(lse.cpu().numpy() - rl).max() <= 1e-3
     for x, ref in zip(grads, (rq, rk, rv)):
         assert np.abs(x.cpu().numpy() - ref).max() <= 2e-2
+
+
+def test_rank_steps_emulated_allgather(ra):
+    """The all-gather variant's order (ring_driver.AllGatherDriver): every rank
+    holds all key/value rows before its first step, runs its steps with no
+    exchange, and each key/value shard's dK/dV partials are summed over the
+    ranks onto the shard's owner at the end."""
+    from context_ring_attention_step_gb300.ring_driver import AllGatherDriver, RankCompute
+    W = 4
+    layout, causal = "zigzag", True
+    wl = custom([1500, 300, 77], 4, 2, 128, W, layout, causal, seed=82, name="rank_steps_allgather")
+    q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
+    args = (wl.cu_seqlens, [W] * wl.num_docs, layout, causal, wl.softmax_scale)
+    plan = ra.Plan(wl.cu_seqlens, [W] * wl.num_docs, layout, causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    o_ref, l_ref = ra.ring_attn_fwd(q, k, v, *args, plan=plan, check=True, fused=False)
+    g_ref = ra.ring_attn_bwd(q, k, v, o_ref, do, l_ref, *args, plan=plan, grads_fp32=True, check=True)
+    drv = [AllGatherDriver(plan, r, W) for r in range(W)]
+    own = [_rows(drv[r].ranges[r]) for r in range(W)]
+
+    def local(x, r):
+        y = torch.zeros_like(x)
+        y[own[r]] = x[own[r]]
+        return y
+
+    comp = [RankCompute(plan, r, local(q, r), k.clone(), v.clone()) for r in range(W)]  # K, V gathered
+    for c in comp:
+        c.fwd_begin()
+        for s in range(W):
+            c.fwd_step(s)
+        c.fwd_end()
+    for r, c in enumerate(comp):
+        c.do = local(do, r)
+        c.bwd_begin()
+        for s in range(W):
+            c.bwd_step(s)
+    for j in range(W):  # the per-shard reduction onto the owner
+        for name in ("dk", "dv"):
+            total = sum(getattr(c, name)[own[j]] for c in comp)
+            getattr(comp[j], name)[own[j]] = total
+    torch.cuda.synchronize()
+    for c in comp:
+        assert ra.workspace_status(c.ws_f) == 0 and ra.workspace_status(c.ws_b) == 0
+    for r, c in enumerate(comp):
+        rows = own[r]
+        assert torch.equal(c.o[rows], o_ref[rows]), r
+        assert torch.equal(c.lse[:, rows], l_ref[:, rows]), r
+        for name, x, ref in zip(("dq", "dk", "dv"), (c.dq, c.dk, c.dv), g_ref):
+            err = (x[rows] - ref[rows]).abs().max().item()
+            assert err <= 1e-5, (r, name, err)
