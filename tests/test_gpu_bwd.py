@@ -80,6 +80,14 @@ def test_cta_pair_backward_ragged_gqa(ra, layout, causal):
     _check_vs_oracle(ra, wl, pairs=True)
 
 
+def test_cta_pair_backward_tiny_documents(ra):
+    """CTA pairs where most ranges hold one key tile or less (the second
+    tile of the pair empty), no GQA grouping (Hq = Hkv)."""
+    wl = custom([1, 5, 130, 129, 257, 3, 64], 2, 2, 128, [1, 1, 2, 1, 3, 1, 2], "zigzag", True, seed=28,
+                name="pairs_tiny_docs")
+    _check_vs_oracle(ra, wl, pairs=True)
+
+
 def test_cta_pair_backward_equals_single_cta(ra):
     """Same gradients from the CTA-pair backward as from the one-CTA kernel,
     within fp32 accumulation-order differences (fp32 gradients)."""

@@ -35,14 +35,18 @@ def _rows(ranges):
     return torch.cat(idx).cuda() if idx else torch.zeros(0, dtype=torch.long, device="cuda")
 
 
-@pytest.mark.parametrize("layout,causal", [("zigzag", True), ("contiguous", True), ("zigzag", False)])
-def test_rank_steps_emulated_ring(ra, layout, causal):
+@pytest.mark.parametrize("layout,causal,pairs", [("zigzag", True, False), ("contiguous", True, False),
+                                                ("zigzag", False, False), ("zigzag", True, True)])
+def test_rank_steps_emulated_ring(ra, layout, causal, pairs):
+    """pairs: the backward on CTA pairs, so each rank's work list must keep
+    its key tiles two by two."""
     from context_ring_attention_step_gb300.ring_driver import RankCompute, RingDriver
     W = 4
     wl = custom([1500, 300, 77], 4, 2, 128, W, layout, causal, seed=81, name="rank_steps")
     q, k, v, do = (x.cuda() for x in draw_qkvdo(wl))
     args = (wl.cu_seqlens, [W] * wl.num_docs, layout, causal, wl.softmax_scale)
-    plan = ra.Plan(wl.cu_seqlens, [W] * wl.num_docs, layout, causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan = ra.Plan(wl.cu_seqlens, [W] * wl.num_docs, layout, causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale,
+                   bwd_cta_pairs=pairs)
     o_ref, l_ref = ra.ring_attn_fwd(q, k, v, *args, plan=plan, check=True, fused=False)
     g_ref = ra.ring_attn_bwd(q, k, v, o_ref, do, l_ref, *args, plan=plan, grads_fp32=True, check=True)
     drv = [RingDriver(plan, r, W) for r in range(W)]
