@@ -845,7 +845,7 @@ ra_status ra_bwd_prepare(const ra_plan* P, const void* o, int32_t o_is_fp32, con
   e = cudaMemsetAsync(ws + L.delta, 0, L.dq ? L.dq - L.delta : L.total - L.delta, st);
   if (e != cudaSuccess) return cuda_fail(e, "stat reset");
   e = ra::launch_bwd_preprocess(o, o_is_fp32, dout, lse, const_cast<float*>(p.delta), const_cast<float*>(p.lse2),
-                                P->T, p.stat_pitch, P->Hq, P->D, st);
+                                P->T, p.stat_pitch, P->Hq, P->D, P->D == 256 ? p.scale : 1.f, st);
   if (e != cudaSuccess) return cuda_fail(e, "backward preprocess launch");
   const size_t nq = (size_t)P->T * P->Hq * P->D, nk = (size_t)P->T * P->Hkv * P->D;
   e = cudaMemsetAsync(p.dq_acc, 0, nq * 4, st);

@@ -86,7 +86,7 @@ __device__ __forceinline__ void load8(const void* base, size_t elem, bool fp32, 
 template <int D>
 __global__ void bwd_preprocess_kernel(const void* __restrict__ o, int o_fp32, const void* __restrict__ dout,
                                       const float* __restrict__ lse, float* __restrict__ delta,
-                                      float* __restrict__ lse2, int T, int64_t pitch, int Hq) {
+                                      float* __restrict__ lse2, int T, int64_t pitch, int Hq, float scale) {
   const long long rows = (long long)T * Hq;
   const long long row = (blockIdx.x * (long long)blockDim.x + threadIdx.x) >> 3;
   const int sub = threadIdx.x & 7;
@@ -109,7 +109,7 @@ __global__ void bwd_preprocess_kernel(const void* __restrict__ o, int o_fp32, co
   if (row < rows && sub == 0) {
     const int t = (int)(row / Hq), h = (int)(row % Hq);
     const size_t idx = (size_t)h * pitch + t;
-    delta[idx] = -acc;
+    delta[idx] = -acc * scale;
     lse2[idx] = -lse[(size_t)h * T + t] * kLog2e;
   }
 }
@@ -140,17 +140,18 @@ cudaError_t launch_ws_init(void* header, size_t header_bytes, const void* src0, 
 }
 
 cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout, const float* lse, float* delta,
-                                  float* lse2, int T, int64_t pitch, int Hq, int D, cudaStream_t stream) {
+                                  float* lse2, int T, int64_t pitch, int Hq, int D, float scale,
+                                  cudaStream_t stream) {
   const long long threads_needed = (long long)T * Hq * 8;
   if (threads_needed == 0) return cudaSuccess;
   const int threads = 256;
   const unsigned blocks = (unsigned)((threads_needed + threads - 1) / threads);
   if (D == 128)
-    bwd_preprocess_kernel<128><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
+    bwd_preprocess_kernel<128><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq, scale);
   else if (D == 64)
-    bwd_preprocess_kernel<64><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
+    bwd_preprocess_kernel<64><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq, scale);
   else if (D == 256)
-    bwd_preprocess_kernel<256><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq);
+    bwd_preprocess_kernel<256><<<blocks, threads, 0, stream>>>(o, o_is_fp32, dout, lse, delta, lse2, T, pitch, Hq, scale);
   else
     return cudaErrorInvalidValue;
   return cudaGetLastError();

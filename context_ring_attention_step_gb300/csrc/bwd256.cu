@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     };
-    uint64_t pf[16];  // scale P^T of this warpgroup's columns (packed fp32 pairs, masked), for its dS phase
+    uint64_t pf[16];  // P^T of this warpgroup's columns (packed fp32 pairs, masked), for its dS phase
     bool ok = true;
     for (int i = 0; i < npairs && ok; ++i) {
       const uint32_t pi = (uint32_t)i & 1u;
@@ -355,7 +355,7 @@ __global__ void __launch_bounds__(512, 1)
           float p0 = ex2_approx(x0), p1 = ex2_approx(x1);
           if (c0 < cmin || c0 >= cmax) p0 = 0.f;
           if (c0 + 1 < cmin || c0 + 1 >= cmax) p1 = 0.f;
-          pf[x] = f2_mul(f2_pack(p0, p1), scale2);
+          pf[x] = f2_pack(p0, p1);
           w[x] = pack_bf16x2(p0, p1);
         }
         tmem_st16(aPk, w);
@@ -374,14 +374,14 @@ __global__ void __launch_bounds__(512, 1)
         tmem_ld32(aP, r);
         tmem_ld_wait();
         reg_fence32(r);
-        const float4* d4 = reinterpret_cast<const float4*>(stat + 64);  // -Delta
+        const float4* d4 = reinterpret_cast<const float4*>(stat + 64);  // -scale Delta
 #pragma unroll
         for (int x = 0; x < 16; ++x) {
           const int c0 = 32 * wg + 2 * x;
           const float4 d = d4[c0 >> 2];
           const uint64_t nd = (x & 1) ? f2_pack(d.z, d.w) : f2_pack(d.x, d.y);
           float v0, v1;
-          f2_unpack(f2_mul(f2_add(f2_pack(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), nd), pf[x]), v0,
+          f2_unpack(f2_mul(f2_fma(f2_pack(__uint_as_float(r[2 * x]), __uint_as_float(r[2 * x + 1])), scale2, nd), pf[x]), v0,
                     v1);
           w[x] = pack_bf16x2(v0, v1);
         }

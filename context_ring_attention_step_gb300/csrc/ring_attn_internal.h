@@ -60,7 +60,7 @@ struct BwdParams {
   float scale_log2;    // softmax scale * log2(e)
   float scale;         // softmax scale
   const float* lse2;   // [Hq, stat_pitch] LSE * log2(e)
-  const float* delta;  // [Hq, stat_pitch] rowsum(dO * O)
+  const float* delta;  // [Hq, stat_pitch] -rowsum(dO * O), times the softmax scale at head_dim 256
   int64_t stat_pitch;  // T rounded up to a multiple of 4
   float* dq_acc;       // fp32 [T, Hq, D], scaled dq accumulated with bulk reductions
   float* dk_acc;       // fp32 [T, Hkv, D]
@@ -100,10 +100,12 @@ cudaError_t launch_bwd_step_d256(const CUtensorMap& tq, const CUtensorMap& tk, c
 // o (bf16) = o_run (fp32), elementwise.
 cudaError_t launch_cast_bf16(const float* src, void* dst, size_t n, cudaStream_t stream);
 cudaError_t launch_wait_timeout_probe(int* status, uint64_t limit_ns, int site, cudaStream_t stream);
-// Delta[h, t] = sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = lse[h, t] * log2(e);
+// delta[h, t] = -s * sum_d dO[t,h,d] * O[t,h,d];  lse2[h, t] = -lse[h, t] * log2(e)
+// (negated, as the backward's compute phases consume them; s = the softmax
+// scale at head_dim 256, whose dS phase folds the scale into one fma, else 1);
 // both written with row pitch `pitch` (>= T).
 cudaError_t launch_bwd_preprocess(const void* o, int o_is_fp32, const void* dout, const float* lse,
-                                  float* delta, float* lse2, int T, int64_t pitch, int Hq, int D,
+                                  float* delta, float* lse2, int T, int64_t pitch, int Hq, int D, float scale,
                                   cudaStream_t stream);
 
 }  // namespace ra
