@@ -1,7 +1,8 @@
 """GPU edge cases against the fp64 oracle: empty documents inside cu_seqlens,
 a single token, more ring shards than tokens (empty shards), a token count
 that is not a multiple of 4 (the padded LSE/Delta rows), for the ring-step
-forward, the single-launch forward and the backward.  Tolerances as in the
+forward, the single-launch forward and the backward, at head_dim 64, 128
+(with the one-CTA and the CTA-pair backward) and 256.  Tolerances as in the
 other parity tests: 2e-2 on fp32 outputs, 1e-3 on LSE."""
 
 import numpy as np
@@ -33,16 +34,21 @@ def ra():
     return m
 
 
+VARIANTS = [("d64", 64, False), ("d128", 128, False), ("d128_pairs", 128, True), ("d256", 256, False)]
+
+
+@pytest.mark.parametrize("variant", VARIANTS, ids=[v[0] for v in VARIANTS])
 @pytest.mark.parametrize("layout", ["zigzag", "contiguous"])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
-def test_edge_case(ra, case, layout, causal):
+def test_edge_case(ra, case, layout, causal, variant):
     name, lengths, cps = case
-    wl = custom(lengths, 4, 2, 64, cps, layout, causal, seed=31, name=name)
+    _, d, pairs = variant
+    wl = custom(lengths, 4, 2, d, cps, layout, causal, seed=31, name=name)
     q, k, v, do = draw_qkvdo(wl)
     rq, rk, rv, ro, rl = A.attention_bwd(q, k, v, do, wl.cu_seqlens, causal, wl.softmax_scale)
     qd, kd, vd, dod = (x.cuda() for x in (q, k, v, do))
-    plan = ra.Plan(wl.cu_seqlens, cps, layout, causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale)
+    plan = ra.Plan(wl.cu_seqlens, cps, layout, causal, wl.Hq, wl.Hkv, wl.d, wl.softmax_scale, bwd_cta_pairs=pairs)
     for fused in (False, True):
         o, lse = ra.ring_attn_fwd(qd, kd, vd, wl.cu_seqlens, cps, layout, causal, wl.softmax_scale, o_fp32=True,
                                   plan=plan, check=True, fused=fused)
